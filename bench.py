@@ -1,0 +1,431 @@
+"""Benchmark of the fine-grained FP8 GEMM path on B300.
+
+One step is one pass of the path over the dense prefill workload
+(M=4096 tokens, K=7168, weights N in {2112, 24576, 7168, 4096}; the shapes of
+the DeepGEMM article's Table 1 and the DeepSeek-V3 prefill): 1x128
+quantization of the BF16 activations, 128x128 quantization of each BF16
+weight, and one FP8 GEMM per weight with FP32 promotion and BF16 output.
+
+Printed metric: FP8 GEMM TFLOP/s of the whole step (2*M*N*K summed over the
+four weights, divided by the step time), with the GEMM kernel's roofline
+fraction (against the FP8 tensor peak) and the quantizers' HBM fraction.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--all]
+With N>1 (torchrun), every rank runs the same workload on its own GPU
+(independent replicas: the path has no exchange step); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+M_PREFILL, K_PREFILL = 4096, 7168
+N_PREFILL = (2112, 24576, 7168, 4096)
+METRIC = "FP8 block-scaled GEMM TFLOP/s & % of B300 FP8 peak; quant GB/s vs HBM"
+FP8_PER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor rate ratio (4.5 / 2.25 PFLOP/s)
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+# DRAM traffic per GEMM launch measured with ncu for the kernel source whose
+# hash is given (dram__bytes_read.sum + dram__bytes_write.sum, per N). When
+# the kernel source changes the hash no longer matches and traffic is null.
+NCU_TRAFFIC = {"kernel_sha": None, "bytes_per_step": None}
+
+
+# ---------------------------------------------------------------- models
+def gemm_flops(M, N, K):
+    return 2.0 * M * N * K
+
+
+def gemm_bytes(M, N, K, out_bytes=2):
+    """Algorithmic bytes of one GEMM: FP8 A and B once, scales once, C once."""
+    return M * K + N * K + M * (K // 128) * 4 + ((N + 127) // 128) * (K // 128) * 4 + M * N * out_bytes
+
+
+def quant_1x128_bytes(M, K, in_bytes=2):
+    return M * K * in_bytes + M * K + M * (K // 128) * 4
+
+
+def quant_128x128_bytes(N, K, in_bytes=2):
+    return N * K * in_bytes + N * K + ((N + 127) // 128) * (K // 128) * 4
+
+
+def table1_gbs(M, N, K, tflops):
+    """Table 1's byte model (FP8 A and B, BF16 C) over the time its TFLOPS implies."""
+    t = gemm_flops(M, N, K) / (tflops * 1e12)
+    return (M * K + N * K + 2 * M * N) / t / 1e9
+
+
+def kernel_sha():
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "fp8_fine_grained_24_b300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append(parts)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------- our arm
+class PrefillStep:
+    """Device-resident buffers and the launches of one step."""
+
+    def __init__(self, fg, torch, device, seed=1001):
+        import workloads as wl
+        self.fg, self.torch = fg, torch
+        M, K = M_PREFILL, K_PREFILL
+        self.x = wl.activations(M, K, seed, device=device)
+        self.w = [wl.weights((n, K), seed + 1 + i, device=device) for i, n in enumerate(N_PREFILL)]
+        self.qa = torch.empty((M, K), dtype=torch.uint8, device=device)
+        self.sa = torch.empty((K // 128, fg.scale_ld(M)), dtype=torch.float32, device=device)
+        self.qb = [torch.empty((n, K), dtype=torch.uint8, device=device) for n in N_PREFILL]
+        self.sb = [torch.empty(((n + 127) // 128, K // 128), dtype=torch.float32, device=device) for n in N_PREFILL]
+        self.c = [torch.empty((M, n), dtype=torch.bfloat16, device=device) for n in N_PREFILL]
+        self.flops = sum(gemm_flops(M, n, K) for n in N_PREFILL)
+        self.launches = 1 + 2 * len(N_PREFILL)
+
+    def run(self, events=None):
+        """Enqueue one step; if `events` is a list, append (kind, start, end) event pairs."""
+        fg, torch = self.fg, self.torch
+
+        def timed(kind, fn):
+            if events is None:
+                fn()
+                return
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            fn()
+            e.record()
+            events.append((kind, s, e))
+
+        timed("quant_1x128", lambda: fg.fp8_quant_1x128_out(self.x, self.qa, self.sa))
+        for i in range(len(N_PREFILL)):
+            timed("quant_128x128", lambda i=i: fg.fp8_quant_128x128_out(self.w[i], self.qb[i], self.sb[i]))
+            timed("gemm", lambda i=i: fg.fp8_gemm_dense_out(self.qa, self.sa, self.qb[i], self.sb[i], self.c[i]))
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import fp8_fine_grained_24_b300 as fg
+
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    step = PrefillStep(fg, torch, device)
+    for _ in range(args.warmup):
+        step.run()
+    fg.check()
+    barrier()
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    events = []
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    start.record()
+    for _ in range(args.steps):
+        step.run(events)
+    end.record()
+    barrier()
+    clocks.stop()
+    fg.check()
+    total_ms = start.elapsed_time(end)
+    per_kind = {}
+    for kind, s, e in events:
+        per_kind.setdefault(kind, []).append(s.elapsed_time(e))
+    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+
+    # ---- end to end through the public API with host buffers
+    e2e = run_e2e(step, fg, torch, device, max(2, min(args.steps, 5)), barrier)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return None
+
+    peaks, peak_src = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_PER_BF16
+    fp8_peak_sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * FP8_PER_BF16
+    gemm_ms = sum(per_kind["gemm"])
+    gemm_tflops = step.flops * args.steps / (gemm_ms * 1e-3) / 1e12
+    q1_ms = sum(per_kind["quant_1x128"])
+    q2_ms = sum(per_kind["quant_128x128"])
+    q1_gbs = quant_1x128_bytes(M_PREFILL, K_PREFILL) * args.steps / (q1_ms * 1e-3) / 1e9
+    q2_gbs = sum(quant_128x128_bytes(n, K_PREFILL) for n in N_PREFILL) * args.steps / (q2_ms * 1e-3) / 1e9
+    sha = kernel_sha()
+    traffic = None
+    if NCU_TRAFFIC["kernel_sha"] == sha and NCU_TRAFFIC["bytes_per_step"]:
+        traffic = NCU_TRAFFIC["bytes_per_step"] / len(N_PREFILL)
+    value = step.flops * world / (ms_per_step * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3 (fp32 accumulate, bf16 out)",
+        "data": "synthetic (seeded N(0,1) activations with 1% channels x30, N(0,0.02) weights)",
+        "config": {
+            "workload": "dense prefill: M=4096, K=7168, N in {2112,24576,7168,4096}; bf16 in, "
+                        "1x128 + 128x128 E4M3 quant, FP8 GEMM, bf16 out",
+            "M": M_PREFILL, "K": K_PREFILL, "N": list(N_PREFILL),
+            "l2": "no flush: each step streams ~1.3 GB (> 126 MB L2)",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "bound": "tensor",
+            "achieved": round(gemm_tflops, 1),
+            "peak": round(fp8_peak, 1),
+            "unit": "TFLOP/s",
+            "frac": round(gemm_tflops / fp8_peak, 4),
+            "traffic": traffic,
+            "kernel": "fp8_gemm_kernel<256> (4 launches per step)",
+            "peak_note": f"{peak_src} bf16 burst {peaks['bf16_tflops']} x {FP8_PER_BF16} (nominal FP8/BF16); "
+                         f"sustained-based peak {round(fp8_peak_sus, 1)}",
+        },
+        "kernels": {
+            "gemm_ms_per_step": round(gemm_ms / args.steps, 4),
+            "quant_1x128_ms_per_step": round(q1_ms / args.steps, 4),
+            "quant_1x128_gbs": round(q1_gbs, 1),
+            "quant_128x128_ms_per_step": round(q2_ms / args.steps, 4),
+            "quant_128x128_gbs": round(q2_gbs, 1),
+            "hbm_peak_gbs": peaks["hbm_gbs"],
+            "gemm_per_n_ms": {str(n): round(statistics.mean(per_kind["gemm"][i::len(N_PREFILL)]), 4)
+                              for i, n in enumerate(N_PREFILL)},
+        },
+        "e2e": e2e,
+        "gpu_launches": step.launches * args.steps,
+        "clocks": clocks.summary(),
+        "kernel_sha": sha,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if dist is not None:
+        dist.destroy_process_group()
+    return line
+
+
+def run_e2e(step, fg, torch, device, steps, barrier):
+    """Same step through the public API, with pinned host inputs copied in and outputs copied out."""
+    hx = step.x.cpu().pin_memory()
+    hw = [w.cpu().pin_memory() for w in step.w]
+    hc = [torch.empty(c.shape, dtype=c.dtype, pin_memory=True) for c in step.c]
+    h2d = hx.numel() * hx.element_size() + sum(w.numel() * w.element_size() for w in hw)
+    d2h = sum(c.numel() * c.element_size() for c in hc)
+    dx = torch.empty_like(step.x)
+    dw = [torch.empty_like(w) for w in step.w]
+
+    def one():
+        dx.copy_(hx, non_blocking=True)
+        for d, h in zip(dw, hw):
+            d.copy_(h, non_blocking=True)
+        fg.fp8_quant_1x128_out(dx, step.qa, step.sa)
+        for i in range(len(N_PREFILL)):
+            fg.fp8_quant_128x128_out(dw[i], step.qb[i], step.sb[i])
+            fg.fp8_gemm_dense_out(step.qa, step.sa, step.qb[i], step.sb[i], step.c[i])
+            hc[i].copy_(step.c[i], non_blocking=True)
+
+    one()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    barrier()
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": round(step.flops / dt / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(dt * 1e3, 3), "steps": steps}
+
+
+# ---------------------------------------------------------------- oracle arm
+def oracle_sample(seconds_budget=15.0, seed=1001):
+    """Time the oracle on a bounded sample of the prefill workload.
+
+    Sample: R activation rows (1x128 quantization) against one 128-row block
+    of every weight (128x128 quantization), FP64 product of the dequantized
+    operands. R is grown until the run takes about `seconds_budget`.
+    Returns (flops, seconds, description).
+    """
+    import torch
+    import workloads as wl
+    from oracle import gemm, quant
+
+    x = wl.activations(M_PREFILL, K_PREFILL, seed, device="cpu").float().numpy()
+    ws = [wl.weights((128, K_PREFILL), seed + 1 + i, device="cpu").float().numpy() for i in range(len(N_PREFILL))]
+    rows = 64
+    while True:
+        t0 = time.perf_counter()
+        qa, sa = quant.quant_1x128(x[:rows])
+        flops = 0.0
+        for w in ws:
+            qb, sb = quant.quant_128x128(w)
+            gemm.gemm_dense(qa, sa, qb, sb)
+            flops += gemm_flops(rows, 128, K_PREFILL)
+        dt = time.perf_counter() - t0
+        if dt >= seconds_budget / 3 or rows >= M_PREFILL:
+            desc = (f"{rows} activation rows x {len(ws)} weight blocks of 128 rows (K=7168): 1x128 + 128x128 "
+                    f"quantization and FP64 product, numpy")
+            return flops, dt, desc
+        rows = min(M_PREFILL, rows * 2)
+    del torch
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        return int(max(n)) if n else os.cpu_count()
+    except Exception:
+        return os.cpu_count()
+
+
+def cpu_baseline(seconds=15.0):
+    flops, dt, desc = oracle_sample(seconds)
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": desc, "seconds": round(dt, 2), "host_cpus": os.cpu_count()}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    vals = []
+    desc = ""
+    for _ in range(args.warmup):
+        oracle_sample(args.cpu_seconds / 3)
+    t_total = 0.0
+    for _ in range(args.steps):
+        flops, dt, desc = oracle_sample(args.cpu_seconds / 3)
+        vals.append(flops / dt / 1e12)
+        t_total += dt
+    value = statistics.mean(vals)
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_total / args.steps * 1e3, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64 (oracle)",
+        "data": "synthetic",
+        "config": {"workload": "dense prefill: M=4096, K=7168, N in {2112,24576,7168,4096} (bounded sample)",
+                   "M": M_PREFILL, "K": K_PREFILL, "N": list(N_PREFILL)},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, local_rank)
+    if line is not None and rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,245 @@
+"""Python binding of the fine-grained FP8 GEMM library (``libfp8fg.so``).
+
+Argument marshalling only: torch tensors supply device pointers, shapes and
+the current CUDA stream; every step of the computation runs in the library's
+CUDA kernels. The functions carry the names of the C entry points declared
+in ``include/fp8fg.h``; the ``*_out`` variants write into caller-provided
+tensors and allocate nothing.
+
+Importing this package loads the shared library and fails loudly
+(ImportError) if it has not been built: there is no fallback path.
+Build it with ``python -m fp8_fine_grained_24_b300.build``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfp8fg.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -m fp8_fine_grained_24_b300.build` "
+        "(nvcc, sm_103a). The library has no non-CUDA fallback.")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+# ---------------------------------------------------------------- constants
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_UNSUPPORTED_SHAPE = -2
+ERR_MISALIGNED = -3
+ERR_CUDA = -4
+ERR_TIMEOUT = -5
+
+BF16, FP32, E4M3 = 0, 1, 2
+SCALE_BLOCK128, SCALE_ROW = 0, 1
+MASK_ROWS, MASK_K = 0, 1
+
+_c_i64 = ctypes.c_int64
+_c_int = ctypes.c_int
+_c_vp = ctypes.c_void_p
+_c_sz = ctypes.c_size_t
+
+_SIGS = {
+    "fp8fg_scale_ld": (_c_i64, [_c_i64]),
+    "fp8_quant_1x128": (_c_int, [_c_vp, _c_int, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_int, _c_vp]),
+    "fp8_quant_128x128": (_c_int, [_c_vp, _c_int, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_int, _c_vp]),
+    "fp8_requant_128x1": (_c_int, [_c_vp, _c_int, _c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_int,
+                                   _c_vp]),
+    "fp8_gemm_dense": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_int, _c_int, _c_i64, _c_i64, _c_i64,
+                                _c_vp, _c_sz, _c_vp]),
+    "fp8fg_gemm_workspace_size": (_c_sz, [_c_i64, _c_i64, _c_i64]),
+    "fp8_gemm_grouped_contig": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_i64, _c_i64, _c_i64,
+                                         _c_i64, _c_vp]),
+    "fp8_gemm_grouped_masked": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_int, _c_vp, _c_int, _c_int,
+                                         _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_vp]),
+    "fp8fg_check": (_c_int, [_c_vp]),
+    "fp8fg_last_error_string": (ctypes.c_char_p, []),
+    "fp8fg_version": (ctypes.c_char_p, []),
+    "fp8fg_debug_set": (_c_int, [_c_int, _c_i64]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+
+class Fp8fgError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"fp8fg error {code}: {msg}")
+        self.code = code
+
+
+def _check(rc: int):
+    if rc != OK:
+        raise Fp8fgError(rc, lib.fp8fg_last_error_string().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+_DT = {torch.bfloat16: BF16, torch.float32: FP32, torch.uint8: E4M3, torch.float8_e4m3fn: E4M3}
+
+
+def _dtype_code(t):
+    try:
+        return _DT[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}") from None
+
+
+def _as_u8(t):
+    return t.view(torch.uint8) if t.dtype == torch.float8_e4m3fn else t
+
+
+def scale_ld(rows: int) -> int:
+    """Row stride (floats) of per-row scale arrays: rows rounded up to 4."""
+    return int(lib.fp8fg_scale_ld(int(rows)))
+
+
+def version() -> str:
+    return lib.fp8fg_version().decode()
+
+
+def check(stream=None):
+    """Synchronize the stream and raise if a device-side wait timed out."""
+    _check(lib.fp8fg_check(_stream(stream)))
+
+
+def debug_set(key: int, value: int):
+    _check(lib.fp8fg_debug_set(int(key), int(value)))
+
+
+# ---------------------------------------------------------------- quantizers
+def fp8_quant_1x128_out(x, q, s, pow2=False, stream=None):
+    M, K = x.shape
+    _check(lib.fp8_quant_1x128(_ptr(x), _dtype_code(x), M, K, x.stride(0), _ptr(q), _ptr(s), int(bool(pow2)),
+                               _stream(stream)))
+    return q, s
+
+
+def fp8_quant_1x128(x, pow2=False, stream=None):
+    """x [M, K] bf16/fp32 -> (q [M, K] uint8 E4M3, s [K/128, ld(M)] fp32)."""
+    assert x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    s = torch.empty((K // 128, scale_ld(M)), dtype=torch.float32, device=x.device)
+    return fp8_quant_1x128_out(x, q, s, pow2, stream)
+
+
+def fp8_quant_128x128_out(w, q, s, pow2=False, stream=None):
+    w3 = w if w.dim() == 3 else w.unsqueeze(0)
+    G, N, K = w3.shape
+    _check(lib.fp8_quant_128x128(_ptr(w3), _dtype_code(w3), G, N, K, _ptr(q), _ptr(s), int(bool(pow2)),
+                                 _stream(stream)))
+    return q, s
+
+
+def fp8_quant_128x128(w, pow2=False, stream=None):
+    """w [N, K] or [G, N, K] -> (q same shape uint8, s [(G,) ceil(N/128), K/128] fp32)."""
+    assert w.is_contiguous()
+    lead = w.shape[:-2]
+    N, K = w.shape[-2:]
+    q = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+    s = torch.empty((*lead, (N + 127) // 128, K // 128), dtype=torch.float32, device=w.device)
+    return fp8_quant_128x128_out(w, q, s, pow2, stream)
+
+
+def fp8_requant_128x1_out(src, s_src, qT, sT, valid_rows=None, pow2=False, stream=None):
+    src3 = src if src.dim() == 3 else src.unsqueeze(0)
+    G, T, C = src3.shape
+    _check(lib.fp8_requant_128x1(_ptr(_as_u8(src3)), _dtype_code(src3), _ptr(s_src), G, T, C, _ptr(valid_rows),
+                                 _ptr(qT), _ptr(sT), int(bool(pow2)), _stream(stream)))
+    return qT, sT
+
+
+def fp8_requant_128x1(src, s_src=None, valid_rows=None, pow2=False, stream=None):
+    """src [(G,) T, C] E4M3 (with s_src [(G,) C/128, ld(T)]) or bf16/fp32
+    -> (qT [(G,) C, T] uint8, sT [(G,) T/128, ld(C)] fp32)."""
+    assert src.is_contiguous()
+    lead = src.shape[:-2]
+    T, C = src.shape[-2:]
+    qT = torch.empty((*lead, C, T), dtype=torch.uint8, device=src.device)
+    sT = torch.empty((*lead, T // 128, scale_ld(C)), dtype=torch.float32, device=src.device)
+    return fp8_requant_128x1_out(src, s_src, qT, sT, valid_rows, pow2, stream)
+
+
+# ---------------------------------------------------------------- GEMMs
+def gemm_workspace_size(M: int, N: int, K: int) -> int:
+    return int(lib.fp8fg_gemm_workspace_size(M, N, K))
+
+
+def fp8_gemm_dense_out(a, sa, b, sb, c, b_scale_kind=SCALE_BLOCK128, accumulate=False, workspace=None,
+                       stream=None):
+    M, K = a.shape
+    N = b.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.fp8_gemm_dense(_ptr(_as_u8(a)), _ptr(sa), _ptr(_as_u8(b)), _ptr(sb), int(b_scale_kind), _ptr(c),
+                              _dtype_code(c), int(bool(accumulate)), M, N, K, _ptr(workspace), ws_bytes,
+                              _stream(stream)))
+    return c
+
+
+def fp8_gemm_dense(a, sa, b, sb, out_dtype=torch.bfloat16, b_scale_kind=SCALE_BLOCK128, stream=None):
+    """C[M, N] = (a * sa) @ (b * sb)^T with FP32 promotion per 128-K block."""
+    M, K = a.shape
+    N = b.shape[0]
+    c = torch.empty((M, N), dtype=out_dtype, device=a.device)
+    ws = None
+    nbytes = gemm_workspace_size(M, N, K)
+    if nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=a.device)
+    return fp8_gemm_dense_out(a, sa, b, sb, c, b_scale_kind, False, ws, stream)
+
+
+def fp8_gemm_grouped_contig_out(a, sa, b, sb, m_indices, c, stream=None):
+    M_total, K = a.shape
+    E, N, _ = b.shape
+    _check(lib.fp8_gemm_grouped_contig(_ptr(_as_u8(a)), _ptr(sa), _ptr(_as_u8(b)), _ptr(sb), _ptr(m_indices),
+                                       _ptr(c), _dtype_code(c), M_total, N, K, E, _stream(stream)))
+    return c
+
+
+def fp8_gemm_grouped_contig(a, sa, b, sb, m_indices, out_dtype=torch.bfloat16, stream=None):
+    """Grouped-contiguous MoE GEMM; padding rows (m_indices == -1) of C are left unwritten."""
+    c = torch.empty((a.shape[0], b.shape[1]), dtype=out_dtype, device=a.device)
+    return fp8_gemm_grouped_contig_out(a, sa, b, sb, m_indices, c, stream)
+
+
+def fp8_gemm_grouped_masked_out(a, sa, b, sb, masked_m, c, b_scale_kind=SCALE_BLOCK128, mask_dim=MASK_ROWS,
+                                accumulate=False, expected_m=0, stream=None):
+    E, M_max, K = a.shape
+    N = b.shape[1]
+    _check(lib.fp8_gemm_grouped_masked(_ptr(_as_u8(a)), _ptr(sa), _ptr(_as_u8(b)), _ptr(sb), int(b_scale_kind),
+                                       _ptr(masked_m), int(mask_dim), _ptr(c), _dtype_code(c),
+                                       int(bool(accumulate)), E, M_max, N, K, int(expected_m), _stream(stream)))
+    return c
+
+
+def fp8_gemm_grouped_masked(a, sa, b, sb, masked_m, out_dtype=torch.bfloat16, b_scale_kind=SCALE_BLOCK128,
+                            mask_dim=MASK_ROWS, expected_m=0, stream=None):
+    """Grouped-masked MoE GEMM (rows >= masked_m[e] of C[e] unwritten in MASK_ROWS mode)."""
+    E, M_max, _ = a.shape
+    c = torch.empty((E, M_max, b.shape[1]), dtype=out_dtype, device=a.device)
+    return fp8_gemm_grouped_masked_out(a, sa, b, sb, masked_m, c, b_scale_kind, mask_dim, False, expected_m,
+                                       stream)
+
+
+__all__ = [
+    "lib", "LIB_PATH", "Fp8fgError", "scale_ld", "version", "check", "debug_set",
+    "fp8_quant_1x128", "fp8_quant_1x128_out", "fp8_quant_128x128", "fp8_quant_128x128_out",
+    "fp8_requant_128x1", "fp8_requant_128x1_out", "gemm_workspace_size",
+    "fp8_gemm_dense", "fp8_gemm_dense_out", "fp8_gemm_grouped_contig", "fp8_gemm_grouped_contig_out",
+    "fp8_gemm_grouped_masked", "fp8_gemm_grouped_masked_out",
+]

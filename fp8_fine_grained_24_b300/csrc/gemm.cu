@@ -1,0 +1,444 @@
+// FP8 GEMM with fine-grained scaling on fifth-generation tensor cores.
+//
+// What it computes (DeepSeek-V3 report excerpt, page 1, paragraph 3): FP8
+// inputs, partial sums of each 128-wide K block promoted to FP32 registers
+// on the CUDA cores and accumulated there in full FP32, output BF16 or FP32;
+// operands carry 1x128 (activation) and 128x128 (weight) or 128x1 scales.
+//
+// How (sm_103a; the pages' Hopper design with two warpgroups ping-ponging
+// WGMMA and promotion is replaced by):
+//   warp 0      TMA producer: A tile 128x128, B tile BNx128 (both K-major,
+//               128-byte swizzle), the 128 row scales of A and, for per-row
+//               B scales, BN column scales, into an S-stage shared-memory
+//               ring guarded by full/empty mbarriers;
+//   warp 1      MMA issuer: 4 x tcgen05.mma.kind::f8f6f4 (K=32 each) per
+//               128-K block into one of two TMEM accumulator buffers, fresh
+//               per K block (no accumulate across blocks), then commits;
+//   warps 2-9   promotion + epilogue: tcgen05.ld the K block's FP32 partial
+//               sums, acc += (sA[m,kb] * sB[n,kb]) * partial in registers,
+//               release the TMEM buffer; after the last K block convert and
+//               store the tile (BF16 or FP32, optional C += for FP32).
+// The kernel is persistent: one CTA per SM walks output tiles with stride
+// gridDim.x, in M-fastest order so that concurrently running CTAs share the
+// same B tiles in L2. Double-buffered TMEM lets the tensor core run one K
+// block ahead of the promotion warps, and the shared-memory ring lets TMA
+// run S blocks ahead.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fp8fg {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 128;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = (2 + kEpiWarps) * 32;
+
+template <int BN>
+struct Cfg {
+  static constexpr int kStages = 4;
+  static constexpr int kABytes = BM * BK;
+  static constexpr int kBBytes = BN * BK;
+  static constexpr int kSABytes = BM * 4;
+  static constexpr int kSBBytes = BN * 4;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kStages * kABytes;
+  static constexpr int kOffSA = kOffB + kStages * kBBytes;
+  static constexpr int kOffSB = kOffSA + kStages * kSABytes;
+  static constexpr int kOffBar = kOffSB + kStages * kSBBytes;
+  // full[S], empty[S], tmem_full[2], tmem_empty[2], drain
+  static constexpr int kNumBars = 2 * kStages + 5;
+  static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+  static constexpr int kSmem = kOffTmemSlot + 16 + 1024;  // + alignment slack
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kColsPerWarp = BN / 2;  // two epilogue warps share a lane quarter
+  static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM columns must be a power of two");
+  static_assert(kSmem > 116 * 1024, "keep one CTA per SM so the TMEM allocation never waits");
+};
+
+struct KArgs {
+  int mode;
+  int rows, N, K;
+  int tiles_m, tiles_n, num_tiles;
+  int groupsB;
+  int b_row;
+  int out_f32, accumulate;
+  const int32_t* m_indices;
+  const int32_t* masked;
+  const float* sB;
+  int sb_nblk, sb_kblk;
+  void* C;
+  int64_t ldc;
+  int64_t c_group_stride;
+  uint32_t* status;
+  uint64_t wait_limit_ns;
+  int debug_skip_fill;
+};
+
+struct Tile {
+  int gA, gB, gC, m0, n0, kbc;
+  bool skip;
+};
+
+template <int BN>
+__device__ __forceinline__ Tile decode_tile(const KArgs& a, int t) {
+  Tile ti;
+  const int per_group = a.tiles_m * a.tiles_n;
+  const int g = t / per_group;
+  const int r = t - g * per_group;
+  const int mb = r % a.tiles_m;
+  const int nb = r / a.tiles_m;
+  ti.m0 = mb * BM;
+  ti.n0 = nb * BN;
+  ti.kbc = a.K / BK;
+  ti.skip = false;
+  ti.gA = ti.gB = ti.gC = 0;
+  if (a.mode == kModeContig) {
+    const int e = __ldg(a.m_indices + ti.m0);
+    ti.gB = e;
+    ti.skip = (e < 0) || (e >= a.groupsB);
+  } else if (a.mode == kModeMaskedRows) {
+    ti.gA = ti.gB = ti.gC = g;
+    ti.skip = ti.m0 >= __ldg(a.masked + g);
+  } else if (a.mode == kModeMaskedK) {
+    ti.gA = ti.gB = ti.gC = g;
+    int mk = __ldg(a.masked + g);
+    mk = mk < 0 ? 0 : mk;
+    const int kbc = (mk + BK - 1) / BK;
+    ti.kbc = kbc < ti.kbc ? kbc : ti.kbc;
+  }
+  return ti;
+}
+
+// Convert and store one epilogue thread's share of a tile row.
+template <int NC>
+__device__ __forceinline__ void store_row(const KArgs& a, const Tile& ti, int row_in_tile, int col0,
+                                          const float (&acc)[NC]) {
+  const int row = ti.m0 + row_in_tile;
+  if (row >= a.rows) return;
+  if (a.mode == kModeContig && __ldg(a.m_indices + row) < 0) return;
+  if (a.mode == kModeMaskedRows && row >= __ldg(a.masked + ti.gC)) return;
+  const int ncol = a.N - (ti.n0 + col0);  // a multiple of 8 (N % 8 == 0)
+  const int64_t off = static_cast<int64_t>(ti.gC) * a.c_group_stride + static_cast<int64_t>(row) * a.ldc +
+                      ti.n0 + col0;
+  if (a.out_f32) {
+    float* c = static_cast<float*>(a.C) + off;
+#pragma unroll
+    for (int j = 0; j < NC; j += 4) {
+      if (j < ncol) {
+        float4 v = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+        if (a.accumulate) {
+          const float4 o = *reinterpret_cast<const float4*>(c + j);
+          v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+        }
+        *reinterpret_cast<float4*>(c + j) = v;
+      }
+    }
+  } else {
+    __nv_bfloat16* c = static_cast<__nv_bfloat16*>(a.C) + off;
+#pragma unroll
+    for (int j = 0; j < NC; j += 8) {
+      if (j < ncol) {
+        uint4 v;
+        v.x = pack_bf16x2(acc[j], acc[j + 1]);
+        v.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
+        v.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
+        v.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
+        *reinterpret_cast<uint4*>(c + j) = v;
+      }
+    }
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                    const KArgs a) {
+  using C = Cfg<BN>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw + pad;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const uint32_t bar0 = sbase + C::kOffBar;
+  auto full_bar = [&](uint32_t s) { return bar0 + s * 8; };
+  auto empty_bar = [&](uint32_t s) { return bar0 + (S + s) * 8; };
+  auto tfull_bar = [&](uint32_t b) { return bar0 + (2 * S + b) * 8; };
+  auto tempty_bar = [&](uint32_t b) { return bar0 + (2 * S + 2 + b) * 8; };
+  const uint32_t drain_bar = bar0 + (2 * S + 4) * 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmemSlot);
+
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmSA);
+    if (a.b_row) prefetch_tmap(&tmSB);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1 + kEpiWarps);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), kEpiWarps);
+    }
+    mbar_init(drain_bar, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint32_t tx = C::kABytes + C::kBBytes + C::kSABytes + (a.b_row ? C::kSBBytes : 0);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < a.num_tiles && ok; t += gridDim.x) {
+        const Tile ti = decode_tile<BN>(a, t);
+        if (ti.skip) continue;
+        for (int kb = 0; kb < ti.kbc; ++kb, ++it) {
+          const uint32_t s = it % S, ph = (it / S) & 1;
+          if (!mbar_wait(empty_bar(s), ph ^ 1, a.status, kStatusTimeoutProducer, a.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(s), tx);
+          if (static_cast<int>(it) == a.debug_skip_fill) continue;  // test hook: never filled
+          tma_load_3d(sbase + C::kOffA + s * C::kABytes, &tmA, full_bar(s), kb * BK, ti.m0, ti.gA);
+          tma_load_3d(sbase + C::kOffB + s * C::kBBytes, &tmB, full_bar(s), kb * BK, ti.n0, ti.gB);
+          tma_load_3d(sbase + C::kOffSA + s * C::kSABytes, &tmSA, full_bar(s), ti.m0, kb, ti.gA);
+          if (a.b_row)
+            tma_load_3d(sbase + C::kOffSB + s * C::kSBBytes, &tmSB, full_bar(s), ti.n0, kb, ti.gB);
+        }
+      }
+      // No copy may still be landing in shared memory when the CTA exits:
+      // wait (bounded, ignoring the error word) for the last fill of each stage.
+      const uint32_t first = it > static_cast<uint32_t>(S) ? it - S : 0;
+      for (uint32_t i = first; i < it; ++i) {
+        mbar_wait(full_bar(i % S), (i / S) & 1, nullptr, 0, a.wait_limit_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = f8_idesc(BM, BN);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < a.num_tiles && ok; t += gridDim.x) {
+        const Tile ti = decode_tile<BN>(a, t);
+        if (ti.skip) continue;
+        for (int kb = 0; kb < ti.kbc; ++kb, ++it) {
+          const uint32_t s = it % S, ph = (it / S) & 1;
+          const uint32_t buf = it & 1, tph = (it >> 1) & 1;
+          if (!mbar_wait(tempty_bar(buf), tph ^ 1, a.status, kStatusTimeoutMma, a.wait_limit_ns) ||
+              !mbar_wait(full_bar(s), ph, a.status, kStatusTimeoutMma, a.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = kmajor_sw128_desc(sbase + C::kOffA + s * C::kABytes);
+          const uint64_t bd = kmajor_sw128_desc(sbase + C::kOffB + s * C::kBBytes);
+          const uint32_t d = tmem_base + buf * BN;
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k) {
+            // advance 32 bytes (= 32 E4M3 elements) along K inside the swizzle atom
+            mma_f8f6f4(d, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
+          }
+          mma_commit(empty_bar(s));
+          mma_commit(tfull_bar(buf));
+        }
+      }
+      // All MMAs issued by this thread complete before TMEM is released.
+      mma_commit(drain_bar);
+      if (!mbar_wait(drain_bar, 0, nullptr, 0, a.wait_limit_ns)) atomicCAS(a.status, 0u, kStatusTimeoutDrain);
+    }
+  } else {
+    // ------------------------------------------------------------ promotion + epilogue
+    constexpr int NC = C::kColsPerWarp;
+    const int quarter = warp & 3;               // TMEM lanes this warp may access
+    const int col0 = ((warp - 2) >> 2) * NC;    // column half of the tile
+    const int row_in_tile = quarter * 32 + lane;
+    const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
+    const float* smem_sa = reinterpret_cast<const float*>(smem + C::kOffSA);
+    const float* smem_sb = reinterpret_cast<const float*>(smem + C::kOffSB);
+    float acc[NC];
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < a.num_tiles && ok; t += gridDim.x) {
+      const Tile ti = decode_tile<BN>(a, t);
+      if (ti.skip) continue;
+#pragma unroll
+      for (int j = 0; j < NC; ++j) acc[j] = 0.0f;
+      for (int kb = 0; kb < ti.kbc; ++kb, ++it) {
+        const uint32_t s = it % S, ph = (it / S) & 1;
+        const uint32_t buf = it & 1, tph = (it >> 1) & 1;
+        float sb_blk = 0.0f;
+        if (!a.b_row) {
+          const int nbk = (ti.n0 + col0) / 128;
+          if (nbk < a.sb_nblk)
+            sb_blk = __ldg(a.sB + (static_cast<int64_t>(ti.gB) * a.sb_nblk + nbk) * a.sb_kblk + kb);
+        }
+        bool got = mbar_wait(tfull_bar(buf), tph, a.status, kStatusTimeoutEpilogue, a.wait_limit_ns);
+        got = got && mbar_wait(full_bar(s), ph, a.status, kStatusTimeoutEpilogue, a.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        const float sa = smem_sa[s * BM + row_in_tile];
+        tc_fence_after();
+#pragma unroll
+        for (int ch = 0; ch < NC / 16; ++ch) {
+          uint32_t r[16];
+          tmem_ld16(tmem_base + lane_bits + buf * BN + col0 + ch * 16, r);
+          if (!a.b_row) {
+            const float sc = sa * sb_blk;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[ch * 16 + j] = fmaf(__uint_as_float(r[j]), sc, acc[ch * 16 + j]);
+          } else {
+            const float* sbv = smem_sb + s * BN + col0 + ch * 16;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              acc[ch * 16 + j] = fmaf(__uint_as_float(r[j]) * sbv[j], sa, acc[ch * 16 + j]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(empty_bar(s));
+          mbar_arrive(tempty_bar(buf));
+        }
+      }
+      if (!ok) break;
+      if (!(a.accumulate && ti.kbc == 0)) store_row<NC>(a, ti, row_in_tile, col0, acc);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+              uint64_t stride1, uint64_t stride2, uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1, stride2};
+  const cuuint32_t box[3] = {b0, b1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int64_t ld4(int64_t r) { return (r + 3) / 4 * 4; }
+
+template <int BN>
+cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limit_ns, int debug_skip_fill,
+                      int num_sms, cudaStream_t stream, const char** detail) {
+  using C = Cfg<BN>;
+  const int64_t KB = p.K / BK;
+  const int64_t groupsA = (p.mode == kModeMaskedRows || p.mode == kModeMaskedK) ? p.groups : 1;
+  CUtensorMap tmA, tmB, tmSA, tmSB;
+  bool ok = make_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.A, p.K, p.rows, groupsA, p.K, p.rows * p.K, BK, BM,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.B, p.K, p.N, p.groupsB, p.K, p.N * p.K, BK, BN,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map(&tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.sA, p.rows, KB, groupsA, ld4(p.rows) * 4,
+                      KB * ld4(p.rows) * 4, BM, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (p.b_row) {
+    ok = ok && make_map(&tmSB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.sB, p.N, KB, p.groupsB, ld4(p.N) * 4,
+                        KB * ld4(p.N) * 4, BN, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+  } else {
+    tmSB = tmSA;  // unused
+  }
+  if (!ok) {
+    *detail = "cuTensorMapEncodeTiled failed (driver entry point missing or arguments rejected)";
+    return cudaErrorInvalidValue;
+  }
+  KArgs a;
+  a.mode = p.mode;
+  a.rows = static_cast<int>(p.rows);
+  a.N = static_cast<int>(p.N);
+  a.K = static_cast<int>(p.K);
+  a.tiles_m = static_cast<int>((p.rows + BM - 1) / BM);
+  a.tiles_n = static_cast<int>((p.N + BN - 1) / BN);
+  const int64_t nt = p.groups * a.tiles_m * a.tiles_n;
+  if (nt > 0x7FFFFFFF) {
+    *detail = "too many output tiles";
+    return cudaErrorInvalidValue;
+  }
+  a.num_tiles = static_cast<int>(nt);
+  a.groupsB = static_cast<int>(p.groupsB);
+  a.b_row = p.b_row;
+  a.out_f32 = p.out_f32;
+  a.accumulate = p.accumulate;
+  a.m_indices = p.m_indices;
+  a.masked = p.masked;
+  a.sB = p.sB;
+  a.sb_nblk = static_cast<int>((p.N + 127) / 128);
+  a.sb_kblk = static_cast<int>(KB);
+  a.C = p.C;
+  a.ldc = p.N;
+  a.c_group_stride = p.rows * p.N;
+  a.status = status;
+  a.wait_limit_ns = wait_limit_ns;
+  a.debug_skip_fill = debug_skip_fill;
+  if (a.num_tiles == 0) return cudaSuccess;
+
+  static int attr_done[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(fp8_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) {
+      *detail = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+      return e;
+    }
+    attr_done[dev] = 1;
+  }
+  const int grid = a.num_tiles < num_sms ? a.num_tiles : num_sms;
+  fp8_gemm_kernel<BN><<<grid, kThreads, C::kSmem, stream>>>(tmA, tmB, tmSA, tmSB, a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) *detail = "GEMM kernel launch failed";
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmProblem& p, uint32_t* status, uint64_t wait_limit_ns, int debug_skip_fill,
+                        int num_sms, cudaStream_t stream, const char** detail) {
+  return launch_bn<256>(p, status, wait_limit_ns, debug_skip_fill, num_sms, stream, detail);
+}
+
+}  // namespace fp8fg

@@ -1,0 +1,47 @@
+// Internal launchers (host side); the public C ABI lives in include/fp8fg.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fp8fg {
+
+cudaError_t launch_quant_1x128(const void* x, bool f32, int64_t M, int64_t K, int64_t ldx, uint8_t* q, float* s,
+                               int64_t lds, int pow2, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_quant_128x128(const void* w, bool f32, int64_t G, int64_t N, int64_t K, uint8_t* q, float* s,
+                                 int pow2, cudaStream_t stream);
+
+// src_kind: 0 E4M3 (+ s_src with row stride ld_t), 1 BF16, 2 FP32
+cudaError_t launch_requant_128x1(const void* src, int src_kind, const float* s_src, int64_t ld_t, int64_t G,
+                                 int64_t T, int64_t C, const int32_t* valid_rows, uint8_t* qT, float* sT,
+                                 int64_t ld_c, int pow2, cudaStream_t stream);
+
+// Scheduling modes of the GEMM kernel.
+enum GemmMode : int { kModeDense = 0, kModeContig = 1, kModeMaskedRows = 2, kModeMaskedK = 3 };
+
+struct GemmProblem {
+  int mode;
+  const uint8_t* A;      // [groupsA][rows][K]
+  const float* sA;       // [groupsA][K/128][ld(rows)]
+  const uint8_t* B;      // [groupsB][N][K]
+  const float* sB;       // block: [groupsB][ceil(N/128)][K/128]; row: [groupsB][K/128][ld(N)]
+  int b_row;             // 1: per-row (128x1) B scales
+  void* C;               // [groupsC][rows][N]
+  int out_f32;
+  int accumulate;
+  int64_t rows;          // rows of A (and C) per group
+  int64_t N, K;
+  int64_t groups;        // groups of tiles (masked modes: E; otherwise 1)
+  int64_t groupsB;       // groups of B (contig: E; masked: E; dense: 1)
+  const int32_t* m_indices;
+  const int32_t* masked;
+};
+
+// Enqueue the GEMM. `status` is a device word that receives timeout codes.
+// Returns cudaSuccess or the first CUDA error; *detail gets a static message.
+cudaError_t launch_gemm(const GemmProblem& p, uint32_t* status, uint64_t wait_limit_ns, int debug_skip_fill,
+                        int num_sms, cudaStream_t stream, const char** detail);
+
+}  // namespace fp8fg

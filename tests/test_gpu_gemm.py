@@ -1,0 +1,283 @@
+"""GPU parity of the FP8 GEMMs against the oracle's FP64 product (tolerance in parity.py).
+
+Operands are quantized by the oracle (never by the CUDA path) and uploaded;
+the library multiplies them; the oracle multiplies the same dequantized
+operands in FP64.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from oracle import gemm, quant
+from parity import compare_gemm, dev, ld4, pad_rows_scale, to_np32
+
+pytestmark = pytest.mark.gpu
+
+
+def _quant_a(x, pow2=False):
+    q, s = quant.quant_1x128(to_np32(x), pow2)
+    M = q.shape[0]
+    return q, s, dev(q), dev(pad_rows_scale(s, M))
+
+
+def _quant_b(w, pow2=False):
+    q, s = quant.quant_128x128(to_np32(w), pow2)
+    return q, s, dev(q), dev(s)
+
+
+def _dense_case(fg, M, N, K, seed, out_dtype=torch.bfloat16, a_dtype=torch.bfloat16):
+    x = wl.activations(M, K, seed, device="cpu", dtype=a_dtype)
+    w = wl.weights((N, K), seed + 1, device="cpu")
+    qa, sa, qa_d, sa_d = _quant_a(x)
+    qb, sb, qb_d, sb_d = _quant_b(w)
+    c = fg.fp8_gemm_dense(qa_d, sa_d, qb_d, sb_d, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    cref = gemm.gemm_dense(qa, sa, qb, sb)
+    return compare_gemm(c, cref, out_dtype == torch.bfloat16)
+
+
+def test_dense_tiny_config(lib):
+    a, b = wl.tiny_inputs(1000, device="cpu")
+    qa, sa, qa_d, sa_d = _quant_a(a)
+    qb, sb, qb_d, sb_d = _quant_b(b)
+    c = lib.fp8_gemm_dense(qa_d, sa_d, qb_d, sb_d)
+    torch.cuda.synchronize()
+    compare_gemm(c, gemm.gemm_dense(qa, sa, qb, sb), True)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (200, 264, 384), (1, 8, 128), (64, 2112, 1024),
+                                   (300, 520, 640), (513, 768, 256), (128, 7168, 2048)])
+def test_dense_shapes(lib, M, N, K):
+    _dense_case(lib, M, N, K, seed=M * 7 + N)
+
+
+def test_dense_fp32_out_and_accumulate(lib):
+    M, N, K = 192, 320, 512
+    x = wl.activations(M, K, 11, device="cpu")
+    w = wl.weights((N, K), 12, device="cpu")
+    qa, sa, qa_d, sa_d = _quant_a(x)
+    qb, sb, qb_d, sb_d = _quant_b(w)
+    cref = gemm.gemm_dense(qa, sa, qb, sb)
+    c = lib.fp8_gemm_dense(qa_d, sa_d, qb_d, sb_d, out_dtype=torch.float32)
+    compare_gemm(c, cref, False)
+    base = torch.randn((M, N), dtype=torch.float32, device="cuda")
+    c2 = base.clone()
+    lib.fp8_gemm_dense_out(qa_d, sa_d, qb_d, sb_d, c2, accumulate=True)
+    compare_gemm(c2, cref + base.double().cpu().numpy(), False)
+
+
+def _wgrad_operands(T, N, C, seed, valid=None):
+    """G [T, N] bf16 and X [T, C] bf16 -> oracle 128x1 pow2 operands (transposed)."""
+    g = wl.normal((T, N), seed, device="cpu", dtype=torch.bfloat16)
+    x = wl.activations(T, C, seed + 1, device="cpu")
+    qgT, sgT = quant.requant_128x1(to_np32(g), None, valid, True)
+    qxT, sxT = quant.requant_128x1(to_np32(x), None, valid, True)
+    return qgT, sgT, qxT, sxT
+
+
+def test_dense_row_scaled_b_wgrad(lib):
+    T, N, C = 384, 136, 264
+    qgT, sgT, qxT, sxT = _wgrad_operands(T, N, C, 21)
+    c = lib.fp8_gemm_dense(dev(qgT), dev(pad_rows_scale(sgT, N)), dev(qxT), dev(pad_rows_scale(sxT, C)),
+                           out_dtype=torch.float32, b_scale_kind=lib.SCALE_ROW)
+    compare_gemm(c, gemm.wgrad(qgT, sgT, qxT, sxT), False)
+
+
+def test_dense_outputs_stay_in_bounds(lib):
+    # canaries around C: nothing outside [M, N] is written
+    M, N, K = 130, 72, 256
+    x = wl.activations(M, K, 31, device="cpu")
+    w = wl.weights((N, K), 32, device="cpu")
+    qa, sa, qa_d, sa_d = _quant_a(x)
+    qb, sb, qb_d, sb_d = _quant_b(w)
+    buf = torch.full((M + 2, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    c = buf[1:M + 1]
+    lib.fp8_gemm_dense_out(qa_d, sa_d, qb_d, sb_d, c)
+    torch.cuda.synchronize()
+    assert torch.isnan(buf[0]).all() and torch.isnan(buf[M + 1]).all()
+    compare_gemm(c, gemm.gemm_dense(qa, sa, qb, sb), True)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("N", wl.PREFILL_NS)
+def test_dense_prefill_sampled(lib, N):
+    M, K = wl.PREFILL_M, wl.PREFILL_K
+    x = wl.activations(M, K, 1001, device="cuda")
+    w = wl.weights((N, K), 2000 + N, device="cuda")
+    qa_d, sa_d = lib.fp8_quant_1x128(x)
+    qb_d, sb_d = lib.fp8_quant_128x128(w)
+    c = lib.fp8_gemm_dense(qa_d, sa_d, qb_d, sb_d)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(N)
+    rows = np.unique(np.concatenate([[0, M - 1], rng.choice(M, 62, replace=False)]))
+    nblocks = np.unique(np.concatenate([[0, (N - 1) // 128], rng.choice((N + 127) // 128, 2, replace=False)]))
+    # oracle operands from the generator's values only
+    qa, sa = quant.quant_1x128(to_np32(x[rows]))
+    for nb in nblocks:
+        cols = slice(nb * 128, min(N, nb * 128 + 128))
+        qb, sb = quant.quant_128x128(to_np32(w[cols]))
+        cref = gemm.gemm_dense(qa, sa, qb, sb)
+        compare_gemm(c[rows][:, cols], cref, True)
+
+
+# ---------------------------------------------------------------- grouped contiguous
+def _contig_case(fg, counts, N, K, seed, sentinel=True):
+    lay = wl.contig_layout(counts)
+    E = len(counts)
+    x = wl.activations(lay.m_total, K, seed, device="cpu")
+    wl.zero_rows_beyond(x.view(1, lay.m_total, K), [lay.m_total], lay.m_total)
+    x[torch.from_numpy(lay.m_indices < 0)] = 0  # padding rows are zero
+    w = wl.weights((E, N, K), seed + 1, device="cpu")
+    qa, sa, qa_d, sa_d = _quant_a(x)
+    qb, sb, qb_d, sb_d = _quant_b(w)
+    mi = dev(lay.m_indices)
+    c = torch.full((lay.m_total, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    fg.fp8_gemm_grouped_contig_out(qa_d, sa_d, qb_d, sb_d, mi, c)
+    torch.cuda.synchronize()
+    cref = gemm.gemm_grouped_contig(qa, sa, qb, sb, lay.m_indices)
+    real = lay.m_indices >= 0
+    compare_gemm(c[torch.from_numpy(real).cuda()], cref[real], True)
+    if sentinel:
+        assert torch.isnan(c[torch.from_numpy(~real).cuda()]).all(), "padding rows were written"
+
+
+def test_contig_small(lib):
+    _contig_case(lib, np.array([130, 0, 61, 256, 1]), 264, 384, 41)
+
+
+def test_contig_zipf_counts(lib):
+    counts = wl.zipf_counts(2000, 8, 1.1, seed=42)
+    _contig_case(lib, counts, 256, 512, 43)
+
+
+@pytest.mark.slow
+def test_contig_full_sampled(lib):
+    E, tokens, N, K = wl.CONTIG_CASES[0]
+    counts = wl.zipf_counts(tokens, E, 1.1, seed=1004)
+    lay = wl.contig_layout(counts)
+    x = wl.activations(lay.m_total, K, 1005, device="cuda")
+    x[torch.from_numpy(lay.m_indices < 0).cuda()] = 0
+    w = wl.weights((E, N, K), 1006, device="cuda")
+    qa_d, sa_d = lib.fp8_quant_1x128(x)
+    qb_d, sb_d = lib.fp8_quant_128x128(w)
+    c = torch.full((lay.m_total, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lib.fp8_gemm_grouped_contig_out(qa_d, sa_d, qb_d, sb_d, dev(lay.m_indices), c)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    real_rows = np.flatnonzero(lay.m_indices >= 0)
+    rows = np.sort(rng.choice(real_rows, 48, replace=False))
+    qa, sa = quant.quant_1x128(to_np32(x[rows]))
+    for nb in (0, 17, N // 128 - 1):
+        cols = slice(nb * 128, nb * 128 + 128)
+        for e in np.unique(lay.m_indices[rows]):
+            sel = lay.m_indices[rows] == e
+            qb, sb = quant.quant_128x128(to_np32(w[e, cols]))
+            cref = gemm.gemm_dense(qa[sel], sa[:, sel], qb, sb)
+            compare_gemm(c[rows[sel]][:, cols], cref, True)
+    pad = np.flatnonzero(lay.m_indices < 0)
+    assert torch.isnan(c[torch.from_numpy(pad).cuda()]).all()
+
+
+# ---------------------------------------------------------------- grouped masked
+def _masked_case(fg, E, Mmax, N, K, masked, seed):
+    x = wl.activations(E * Mmax, K, seed, device="cpu").view(E, Mmax, K)
+    wl.zero_rows_beyond(x, masked, Mmax)
+    w = wl.weights((E, N, K), seed + 1, device="cpu")
+    qas, sas = zip(*[quant.quant_1x128(to_np32(x[e])) for e in range(E)])
+    qa = np.stack(qas)
+    sa = np.stack(sas)
+    sa_pad = np.stack([pad_rows_scale(s, Mmax) for s in sas])
+    qb, sb = quant.quant_128x128(to_np32(w))
+    c = torch.full((E, Mmax, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    fg.fp8_gemm_grouped_masked_out(dev(qa), dev(sa_pad), dev(qb), dev(sb),
+                                   torch.tensor(masked, dtype=torch.int32, device="cuda"), c)
+    torch.cuda.synchronize()
+    cref = gemm.gemm_grouped_masked(qa, sa, qb, sb, masked)
+    for e in range(E):
+        m = int(masked[e])
+        if m:
+            compare_gemm(c[e, :m], cref[e, :m], True)
+        assert torch.isnan(c[e, m:]).all(), f"expert {e}: rows beyond masked_m written"
+
+
+def test_masked_small(lib):
+    _masked_case(lib, 4, 256, 264, 384, np.array([0, 256, 17, 129], np.int32), 51)
+
+
+def test_masked_decode_like(lib):
+    masked = wl.masked_counts(6, 256, seed=52)
+    _masked_case(lib, 6, 256, 512, 1024, masked, 53)
+
+
+def test_masked_k_wgrad(lib):
+    # per expert dW_e[N, C] = G_e^T X_e over the expert's tokens (K = tokens)
+    E, T, N, C = 3, 384, 136, 264
+    masked = np.array([0, 100, 384], np.int32)
+    qg, sg, qx, sx = [], [], [], []
+    for e in range(E):
+        a, b, c_, d = _wgrad_operands(T, N, C, 60 + e, valid=masked[e])
+        qg.append(a); sg.append(pad_rows_scale(b, N)); qx.append(c_); sx.append(pad_rows_scale(d, C))
+    out = torch.randn((E, N, C), dtype=torch.float32, device="cuda")
+    lib.fp8_gemm_grouped_masked_out(dev(np.stack(qg)), dev(np.stack(sg)), dev(np.stack(qx)), dev(np.stack(sx)),
+                                    torch.tensor(masked, device="cuda"), out, b_scale_kind=lib.SCALE_ROW,
+                                    mask_dim=lib.MASK_K)
+    torch.cuda.synchronize()
+    for e in range(E):
+        ref = gemm.wgrad(qg[e], sg[e][:, :N], qx[e], sx[e][:, :C])
+        if masked[e] == 0:
+            assert torch.count_nonzero(out[e]) == 0
+        else:
+            compare_gemm(out[e], ref, False)
+
+
+@pytest.mark.slow
+def test_masked_full_decode_sampled(lib):
+    E, Mmax, N, K = wl.MASKED_CASE
+    masked = wl.masked_counts(E, Mmax, seed=1007)
+    masked[0] = 0
+    masked[1] = Mmax
+    x = wl.activations(E * Mmax, K, 1008, device="cuda").view(E, Mmax, K)
+    wl.zero_rows_beyond(x, masked, Mmax)
+    w = wl.weights((E, N, K), 1009, device="cuda")
+    qa_d = torch.empty((E, Mmax, K), dtype=torch.uint8, device="cuda")
+    sa_d = torch.empty((E, K // 128, ld4(Mmax)), dtype=torch.float32, device="cuda")
+    for e in range(E):
+        lib.fp8_quant_1x128_out(x[e], qa_d[e], sa_d[e])
+    qb_d, sb_d = lib.fp8_quant_128x128(w)
+    c = torch.full((E, Mmax, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    mm = torch.tensor(masked, dtype=torch.int32, device="cuda")
+    lib.fp8_gemm_grouped_masked_out(qa_d, sa_d, qb_d, sb_d, mm, c, expected_m=128)
+    torch.cuda.synchronize()
+    for e in (1, 5, 15):
+        m = int(masked[e])
+        qa, sa = quant.quant_1x128(to_np32(x[e, :m]))
+        for nb in (0, 31):
+            cols = slice(nb * 128, nb * 128 + 128)
+            qb, sb = quant.quant_128x128(to_np32(w[e, cols]))
+            compare_gemm(c[e, :m, cols], gemm.gemm_dense(qa, sa, qb, sb), True)
+    for e in range(E):
+        assert torch.isnan(c[e, int(masked[e]):]).all()
+
+
+# ---------------------------------------------------------------- bounded waits
+def test_timeout_reports_error_and_context_survives(lib):
+    M, N, K = 128, 256, 512
+    x = wl.activations(M, K, 71, device="cpu")
+    w = wl.weights((N, K), 72, device="cpu")
+    qa, sa, qa_d, sa_d = _quant_a(x)
+    qb, sb, qb_d, sb_d = _quant_b(w)
+    lib.check()
+    try:
+        lib.debug_set(1, 50_000_000)   # 50 ms wait limit
+        lib.debug_set(2, 1)            # the second pipeline fill is never issued
+        lib.fp8_gemm_dense(qa_d, sa_d, qb_d, sb_d)
+        with pytest.raises(lib.Fp8fgError) as ei:
+            lib.check()
+        assert ei.value.code == lib.ERR_TIMEOUT
+    finally:
+        lib.debug_set(2, -1)
+        lib.debug_set(1, 0)
+    c = lib.fp8_gemm_dense(qa_d, sa_d, qb_d, sb_d)
+    lib.check()
+    compare_gemm(c, gemm.gemm_dense(qa, sa, qb, sb), True)
