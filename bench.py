@@ -92,7 +92,12 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index):
-        self.gpu = gpu_index
+        self.gpu = str(gpu_index)
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            ids = [v.strip() for v in vis.split(",")]
+            if gpu_index < len(ids):
+                self.gpu = ids[gpu_index]
         self.samples = []
         self.proc = None
         self.thread = None
@@ -101,7 +106,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
             return
@@ -112,7 +117,10 @@ class ClockSampler:
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) >= 9:
-                self.samples.append(parts)
+                self.samples.append((time.time(), parts))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
 
     def stop(self):
         if self.proc is not None:
@@ -125,8 +133,11 @@ class ClockSampler:
             self.thread.join(timeout=5)
 
     def summary(self):
-        if not self.samples:
+        t0, t1 = getattr(self, "window", (0.0, float("inf")))
+        inside = [p for t, p in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.samples = inside
         sm = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
         mx = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -190,21 +201,24 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
 
     step = PrefillStep(fg, torch, device)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
     for _ in range(args.warmup):
         step.run()
     fg.check()
     barrier()
+    time.sleep(0.3)  # let the sampler start
 
-    clocks = ClockSampler(local_rank)
-    clocks.start()
     events = []
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
+    w0 = time.time()
     start.record()
     for _ in range(args.steps):
         step.run(events)
     end.record()
     barrier()
+    clocks.mark(w0, time.time())
     clocks.stop()
     fg.check()
     total_ms = start.elapsed_time(end)
@@ -406,10 +420,78 @@ def run_reference(args, rank, world):
     }
 
 
+def run_case(args):
+    """Time one kernel on one shape (sweeps and ncu captures): prints one JSON line.
+
+    gemm M,N,K        dense GEMM, bf16 out (operands quantized once, untimed)
+    quant1x128 M,K    activation quantization of bf16 [M, K]
+    quant128x128 N,K  weight quantization of bf16 [N, K]
+    requant T,C       128x1 requantization of an E4M3 [T, C] with 1x128 scales (pow2)
+    """
+    import torch
+    import fp8_fine_grained_24_b300 as fg
+    import workloads as wl
+
+    dims = [int(v) for v in args.shape.split(",")]
+    dev = torch.device("cuda", 0)
+    if args.case == "gemm":
+        M, N, K = dims
+        qa, sa = fg.fp8_quant_1x128(wl.activations(M, K, 1001, device=dev))
+        qb, sb = fg.fp8_quant_128x128(wl.weights((N, K), 1002, device=dev))
+        c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        fn = lambda: fg.fp8_gemm_dense_out(qa, sa, qb, sb, c)  # noqa: E731
+        work, unit, nbytes = gemm_flops(M, N, K), "TFLOP/s", gemm_bytes(M, N, K)
+    elif args.case == "quant1x128":
+        M, K = dims
+        x = wl.activations(M, K, 1001, device=dev)
+        q = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        s = torch.empty((K // 128, fg.scale_ld(M)), dtype=torch.float32, device=dev)
+        fn = lambda: fg.fp8_quant_1x128_out(x, q, s)  # noqa: E731
+        work, unit, nbytes = None, "GB/s", quant_1x128_bytes(M, K)
+    elif args.case == "quant128x128":
+        N, K = dims
+        w = wl.weights((N, K), 1002, device=dev)
+        q = torch.empty((N, K), dtype=torch.uint8, device=dev)
+        s = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=dev)
+        fn = lambda: fg.fp8_quant_128x128_out(w, q, s)  # noqa: E731
+        work, unit, nbytes = None, "GB/s", quant_128x128_bytes(N, K)
+    elif args.case == "requant":
+        T, C = dims
+        qa, sa = fg.fp8_quant_1x128(wl.activations(T, C, 1001, device=dev))
+        qT = torch.empty((C, T), dtype=torch.uint8, device=dev)
+        sT = torch.empty((T // 128, fg.scale_ld(C)), dtype=torch.float32, device=dev)
+        fn = lambda: fg.fp8_requant_128x1_out(qa.view(torch.float8_e4m3fn), sa, qT, sT, pow2=True)  # noqa: E731
+        work, unit, nbytes = None, "GB/s", T * C * 2 + T * (C // 128) * 4 + (T // 128) * C * 4
+    else:
+        raise SystemExit(f"unknown case {args.case}")
+    for _ in range(args.warmup):
+        fn()
+    fg.check()
+    times = []
+    for _ in range(args.steps):
+        s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_.record()
+        fn()
+        e_.record()
+        times.append((s_, e_))
+    torch.cuda.synchronize()
+    fg.check()
+    ms = [a.elapsed_time(b) for a, b in times]
+    med = statistics.median(ms)
+    out = {"case": args.case, "shape": dims, "ms_median": round(med, 5), "ms_min": round(min(ms), 5),
+           "bytes": int(nbytes), "GB/s": round(nbytes / (med * 1e-3) / 1e9, 1)}
+    if work is not None:
+        out["TFLOP/s"] = round(work / (med * 1e-3) / 1e12, 1)
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--case", choices=["gemm", "quant1x128", "quant128x128", "requant"], default=None,
+                    help="time a single kernel on --shape instead of the full step")
+    ap.add_argument("--shape", default="4096,7168,7168")
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -419,6 +501,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.case is not None:
+        run_case(args)
+        return
     if args.impl == "reference":
         line = run_reference(args, rank, world)
     else:

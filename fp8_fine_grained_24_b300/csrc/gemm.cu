@@ -12,19 +12,24 @@
 //               B scales, BN column scales, into an S-stage shared-memory
 //               ring guarded by full/empty mbarriers;
 //   warp 1      MMA issuer: 4 x tcgen05.mma.kind::f8f6f4 (K=32 each) per
-//               128-K block into one of two TMEM accumulator buffers, fresh
-//               per K block (no accumulate across blocks), then commits;
-//   warps 2-9   promotion + epilogue: tcgen05.ld the K block's FP32 partial
+//               128-K block into one of several TMEM accumulator buffers,
+//               fresh per K block (no accumulation across blocks), then
+//               commits to the stage's "empty" and the buffer's "full"
+//               barriers;
+//   warps 2..   promotion + epilogue: tcgen05.ld the K block's FP32 partial
 //               sums, acc += (sA[m,kb] * sB[n,kb]) * partial in registers,
 //               release the TMEM buffer; after the last K block convert and
 //               store the tile (BF16 or FP32, optional C += for FP32).
+// Thread <-> data: each epilogue thread owns one row of the tile (its TMEM
+// lane) and a contiguous group of columns, so the A scale is one scalar per
+// thread per K block and the B block scale one scalar per warp.
 // The kernel is persistent: one CTA per SM walks output tiles with stride
 // gridDim.x, in M-fastest order so that concurrently running CTAs share the
-// same B tiles in L2. Double-buffered TMEM lets the tensor core run one K
-// block ahead of the promotion warps, and the shared-memory ring lets TMA
-// run S blocks ahead.
+// same B tiles in L2. Several TMEM buffers let the tensor core run ahead of
+// the promotion warps; the shared-memory ring lets TMA run S blocks ahead.
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -36,12 +41,18 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 128;
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = (2 + kEpiWarps) * 32;
 
+// Tile configurations. The epilogue warps split the tile's columns in
+// groups of kColsPerWarp; four warps (one per TMEM lane quarter) share a
+// group. Register budget per thread is 65536 / (4 * ceil(warps / 4) * 32).
 template <int BN>
 struct Cfg {
-  static constexpr int kStages = 4;
+  static constexpr int kColsPerWarp = (BN == 256) ? 128 : 64;
+  static constexpr int kEpiWarps = 4 * BN / kColsPerWarp;   // 128: 8, 192: 12, 256: 8
+  static constexpr int kThreads = (2 + kEpiWarps) * 32;
+  static constexpr int kAccBufs = (BN == 128) ? 4 : 2;      // TMEM partial-sum buffers
+  static constexpr int kTmemCols = 512;                      // whole TMEM: one CTA per SM
+  static constexpr int kStages = (BN == 128) ? 6 : (BN == 192 ? 5 : 4);
   static constexpr int kABytes = BM * BK;
   static constexpr int kBBytes = BN * BK;
   static constexpr int kSABytes = BM * 4;
@@ -50,15 +61,18 @@ struct Cfg {
   static constexpr int kOffB = kOffA + kStages * kABytes;
   static constexpr int kOffSA = kOffB + kStages * kBBytes;
   static constexpr int kOffSB = kOffSA + kStages * kSABytes;
-  static constexpr int kOffBar = kOffSB + kStages * kSBBytes;
-  // full[S], empty[S], tmem_full[2], tmem_empty[2], drain
-  static constexpr int kNumBars = 2 * kStages + 5;
+  static constexpr int kOffSbw = kOffSB + kStages * kSBBytes;  // per-warp block-scale staging
+  static constexpr int kSbwChunk = 128;                           // K blocks staged at a time
+  static constexpr int kOffBar = kOffSbw + kEpiWarps * kSbwChunk * 4;
+  // full[S], empty[S], tmem_full[B], tmem_empty[B], drain
+  static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 1;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kSmem = kOffTmemSlot + 16 + 1024;  // + alignment slack
-  static constexpr int kTmemCols = 2 * BN;
-  static constexpr int kColsPerWarp = BN / 2;  // two epilogue warps share a lane quarter
-  static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM columns must be a power of two");
+  static_assert(kAccBufs * BN <= kTmemCols, "TMEM buffers exceed 512 columns");
   static_assert(kSmem > 116 * 1024, "keep one CTA per SM so the TMEM allocation never waits");
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+  static_assert((kOffB % 1024) == 0 && (kABytes % 1024) == 0 && (kBBytes % 1024) == 0,
+                "128-byte swizzled tiles need 1024-byte alignment");
 };
 
 struct KArgs {
@@ -66,8 +80,7 @@ struct KArgs {
   int rows, N, K;
   int tiles_m, tiles_n, num_tiles;
   int groupsB;
-  int b_row;
-  int out_f32, accumulate;
+  int accumulate;
   const int32_t* m_indices;
   const int32_t* masked;
   const float* sB;
@@ -116,7 +129,7 @@ __device__ __forceinline__ Tile decode_tile(const KArgs& a, int t) {
 }
 
 // Convert and store one epilogue thread's share of a tile row.
-template <int NC>
+template <int NC, bool kF32>
 __device__ __forceinline__ void store_row(const KArgs& a, const Tile& ti, int row_in_tile, int col0,
                                           const float (&acc)[NC]) {
   const int row = ti.m0 + row_in_tile;
@@ -126,7 +139,7 @@ __device__ __forceinline__ void store_row(const KArgs& a, const Tile& ti, int ro
   const int ncol = a.N - (ti.n0 + col0);  // a multiple of 8 (N % 8 == 0)
   const int64_t off = static_cast<int64_t>(ti.gC) * a.c_group_stride + static_cast<int64_t>(row) * a.ldc +
                       ti.n0 + col0;
-  if (a.out_f32) {
+  if constexpr (kF32) {
     float* c = static_cast<float*>(a.C) + off;
 #pragma unroll
     for (int j = 0; j < NC; j += 4) {
@@ -155,13 +168,27 @@ __device__ __forceinline__ void store_row(const KArgs& a, const Tile& ti, int ro
   }
 }
 
-template <int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+// acc[j] += partial[j] * sc  (block-scaled B)   or
+// acc[j] += partial[j] * sbv[j] * sa            (per-row B scales)
+template <int W, bool kBRow>
+__device__ __forceinline__ void promote(float* acc, const uint32_t (&r)[W], float sc, float sa, const float* sbv) {
+#pragma unroll
+  for (int j = 0; j < W; ++j) {
+    if constexpr (kBRow)
+      acc[j] = fmaf(__uint_as_float(r[j]) * sbv[j], sa, acc[j]);
+    else
+      acc[j] = fmaf(__uint_as_float(r[j]), sc, acc[j]);
+  }
+}
+
+template <int BN, bool kBRow, bool kF32>
+__global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                     const KArgs a) {
   using C = Cfg<BN>;
   constexpr int S = C::kStages;
+  constexpr int NB = C::kAccBufs;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -172,25 +199,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   const uint32_t bar0 = sbase + C::kOffBar;
-  auto full_bar = [&](uint32_t s) { return bar0 + s * 8; };
-  auto empty_bar = [&](uint32_t s) { return bar0 + (S + s) * 8; };
-  auto tfull_bar = [&](uint32_t b) { return bar0 + (2 * S + b) * 8; };
-  auto tempty_bar = [&](uint32_t b) { return bar0 + (2 * S + 2 + b) * 8; };
-  const uint32_t drain_bar = bar0 + (2 * S + 4) * 8;
+  auto full_bar = [bar0](uint32_t s) { return bar0 + s * 8; };
+  auto empty_bar = [bar0](uint32_t s) { return bar0 + (S + s) * 8; };
+  auto tfull_bar = [bar0](uint32_t b) { return bar0 + (2 * S + b) * 8; };
+  auto tempty_bar = [bar0](uint32_t b) { return bar0 + (2 * S + NB + b) * 8; };
+  const uint32_t drain_bar = bar0 + (2 * S + 2 * NB) * 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmemSlot);
 
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmSA);
-    if (a.b_row) prefetch_tmap(&tmSB);
+    if (kBRow) prefetch_tmap(&tmSB);
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1 + kEpiWarps);
+      mbar_init(empty_bar(s), 1 + C::kEpiWarps);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NB; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), kEpiWarps);
+      mbar_init(tempty_bar(b), C::kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     fence_barrier_init();
@@ -204,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint32_t tx = C::kABytes + C::kBBytes + C::kSABytes + (a.b_row ? C::kSBBytes : 0);
+      constexpr uint32_t tx = C::kABytes + C::kBBytes + C::kSABytes + (kBRow ? C::kSBBytes : 0);
       uint32_t it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < a.num_tiles && ok; t += gridDim.x) {
@@ -221,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sbase + C::kOffA + s * C::kABytes, &tmA, full_bar(s), kb * BK, ti.m0, ti.gA);
           tma_load_3d(sbase + C::kOffB + s * C::kBBytes, &tmB, full_bar(s), kb * BK, ti.n0, ti.gB);
           tma_load_3d(sbase + C::kOffSA + s * C::kSABytes, &tmSA, full_bar(s), ti.m0, kb, ti.gA);
-          if (a.b_row)
+          if (kBRow)
             tma_load_3d(sbase + C::kOffSB + s * C::kSBBytes, &tmSB, full_bar(s), ti.n0, kb, ti.gB);
         }
       }
@@ -243,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ti.skip) continue;
         for (int kb = 0; kb < ti.kbc; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1;
-          const uint32_t buf = it & 1, tph = (it >> 1) & 1;
+          const uint32_t buf = it % NB, tph = (it / NB) & 1;
           if (!mbar_wait(tempty_bar(buf), tph ^ 1, a.status, kStatusTimeoutMma, a.wait_limit_ns) ||
               !mbar_wait(full_bar(s), ph, a.status, kStatusTimeoutMma, a.wait_limit_ns)) {
             ok = false;
@@ -269,12 +296,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ promotion + epilogue
     constexpr int NC = C::kColsPerWarp;
+    const int ew = warp - 2;
     const int quarter = warp & 3;               // TMEM lanes this warp may access
-    const int col0 = ((warp - 2) >> 2) * NC;    // column half of the tile
+    const int col0 = (ew >> 2) * NC;            // column group of the tile
     const int row_in_tile = quarter * 32 + lane;
     const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
     const float* smem_sa = reinterpret_cast<const float*>(smem + C::kOffSA);
     const float* smem_sb = reinterpret_cast<const float*>(smem + C::kOffSB);
+    // Block scales of this warp's column group (inside one 128-column block),
+    // staged 128 K blocks at a time by the warp itself: no cross-warp
+    // barrier that a warp leaving on the error path could leave waiting.
+    float* sbw = reinterpret_cast<float*>(smem + C::kOffSbw) + ew * C::kSbwChunk;
     float acc[NC];
     uint32_t it = 0;
     bool ok = true;
@@ -285,12 +317,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < NC; ++j) acc[j] = 0.0f;
       for (int kb = 0; kb < ti.kbc; ++kb, ++it) {
         const uint32_t s = it % S, ph = (it / S) & 1;
-        const uint32_t buf = it & 1, tph = (it >> 1) & 1;
-        float sb_blk = 0.0f;
-        if (!a.b_row) {
+        const uint32_t buf = it % NB, tph = (it / NB) & 1;
+        if (!kBRow && (kb % C::kSbwChunk) == 0) {
           const int nbk = (ti.n0 + col0) / 128;
-          if (nbk < a.sb_nblk)
-            sb_blk = __ldg(a.sB + (static_cast<int64_t>(ti.gB) * a.sb_nblk + nbk) * a.sb_kblk + kb);
+          const float* src = a.sB + (static_cast<int64_t>(ti.gB) * a.sb_nblk + nbk) * a.sb_kblk;
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < C::kSbwChunk / 32; ++i) {
+            const int k = kb + i * 32 + lane;
+            sbw[i * 32 + lane] = (nbk < a.sb_nblk && k < ti.kbc) ? __ldg(src + k) : 0.0f;
+          }
+          __syncwarp();
         }
         bool got = mbar_wait(tfull_bar(buf), tph, a.status, kStatusTimeoutEpilogue, a.wait_limit_ns);
         got = got && mbar_wait(full_bar(s), ph, a.status, kStatusTimeoutEpilogue, a.wait_limit_ns);
@@ -299,20 +336,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const float sa = smem_sa[s * BM + row_in_tile];
+        float sc = 0.0f;
+        if constexpr (!kBRow) sc = sa * sbw[kb % C::kSbwChunk];
+        const float* sbv = smem_sb + s * BN + col0;
+        const uint32_t taddr = tmem_base + lane_bits + buf * BN + col0;
         tc_fence_after();
+        if constexpr (NC == 64 && C::kThreads <= 320) {
+          uint32_t r[64];
+          tmem_ld64(taddr, r);
+          promote<64, kBRow>(acc, r, sc, sa, sbv);
+        } else if constexpr (NC == 64) {
 #pragma unroll
-        for (int ch = 0; ch < NC / 16; ++ch) {
-          uint32_t r[16];
-          tmem_ld16(tmem_base + lane_bits + buf * BN + col0 + ch * 16, r);
-          if (!a.b_row) {
-            const float sc = sa * sb_blk;
+          for (int ch = 0; ch < 2; ++ch) {
+            uint32_t r[32];
+            tmem_ld32(taddr + ch * 32, r);
+            promote<32, kBRow>(acc + ch * 32, r, sc, sa, sbv + ch * 32);
+          }
+        } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[ch * 16 + j] = fmaf(__uint_as_float(r[j]), sc, acc[ch * 16 + j]);
-          } else {
-            const float* sbv = smem_sb + s * BN + col0 + ch * 16;
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              acc[ch * 16 + j] = fmaf(__uint_as_float(r[j]) * sbv[j], sa, acc[ch * 16 + j]);
+          for (int ch = 0; ch < NC / 16; ++ch) {
+            uint32_t r[16];
+            tmem_ld16(taddr + ch * 16, r);
+            promote<16, kBRow>(acc + ch * 16, r, sc, sa, sbv + ch * 16);
           }
         }
         tc_fence_before();
@@ -323,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      if (!(a.accumulate && ti.kbc == 0)) store_row<NC>(a, ti, row_in_tile, col0, acc);
+      if (!(a.accumulate && ti.kbc == 0)) store_row<NC, kF32>(a, ti, row_in_tile, col0, acc);
     }
   }
 
@@ -400,8 +445,6 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
   }
   a.num_tiles = static_cast<int>(nt);
   a.groupsB = static_cast<int>(p.groupsB);
-  a.b_row = p.b_row;
-  a.out_f32 = p.out_f32;
   a.accumulate = p.accumulate;
   a.m_indices = p.m_indices;
   a.masked = p.masked;
@@ -416,29 +459,43 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
   a.debug_skip_fill = debug_skip_fill;
   if (a.num_tiles == 0) return cudaSuccess;
 
-  static int attr_done[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(fp8_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (e != cudaSuccess) {
-      *detail = "cudaFuncSetAttribute(max dynamic shared memory) failed";
-      return e;
-    }
-    attr_done[dev] = 1;
+  auto kernel = p.b_row ? (p.out_f32 ? fp8_gemm_kernel<BN, true, true> : fp8_gemm_kernel<BN, true, false>)
+                        : (p.out_f32 ? fp8_gemm_kernel<BN, false, true> : fp8_gemm_kernel<BN, false, false>);
+  // the attribute is per function; setting it again is cheap and thread-safe
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) {
+    *detail = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+    return e;
   }
   const int grid = a.num_tiles < num_sms ? a.num_tiles : num_sms;
-  fp8_gemm_kernel<BN><<<grid, kThreads, C::kSmem, stream>>>(tmA, tmB, tmSA, tmSB, a);
-  cudaError_t e = cudaGetLastError();
+  kernel<<<grid, C::kThreads, C::kSmem, stream>>>(tmA, tmB, tmSA, tmSB, a);
+  e = cudaGetLastError();
   if (e != cudaSuccess) *detail = "GEMM kernel launch failed";
   return e;
+}
+
+// Tile width: FP8FG_BN=128|192|256 overrides (tuning); otherwise 256.
+int pick_bn(const GemmProblem& p) {
+  (void)p;
+  static int forced = [] {
+    const char* v = std::getenv("FP8FG_BN");
+    if (!v) return 0;
+    const int b = std::atoi(v);
+    return (b == 128 || b == 192 || b == 256) ? b : 0;
+  }();
+  if (forced) return forced;
+  return 256;
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(const GemmProblem& p, uint32_t* status, uint64_t wait_limit_ns, int debug_skip_fill,
                         int num_sms, cudaStream_t stream, const char** detail) {
-  return launch_bn<256>(p, status, wait_limit_ns, debug_skip_fill, num_sms, stream, detail);
+  switch (pick_bn(p)) {
+    case 192: return launch_bn<192>(p, status, wait_limit_ns, debug_skip_fill, num_sms, stream, detail);
+    case 256: return launch_bn<256>(p, status, wait_limit_ns, debug_skip_fill, num_sms, stream, detail);
+    default: return launch_bn<128>(p, status, wait_limit_ns, debug_skip_fill, num_sms, stream, detail);
+  }
 }
 
 }  // namespace fp8fg
