@@ -439,7 +439,8 @@ def run_case(args):
         qa, sa = fg.fp8_quant_1x128(wl.activations(M, K, 1001, device=dev))
         qb, sb = fg.fp8_quant_128x128(wl.weights((N, K), 1002, device=dev))
         c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        fn = lambda: fg.fp8_gemm_dense_out(qa, sa, qb, sb, c)  # noqa: E731
+        ws = fg.gemm_workspace(M, N, K, device=dev)
+        fn = lambda: fg.fp8_gemm_dense_out(qa, sa, qb, sb, c, workspace=ws)  # noqa: E731
         work, unit, nbytes = gemm_flops(M, N, K), "TFLOP/s", gemm_bytes(M, N, K)
     elif args.case == "quant1x128":
         M, K = dims
@@ -467,19 +468,34 @@ def run_case(args):
     for _ in range(args.warmup):
         fn()
     fg.check()
+    # R calls captured in one CUDA graph: replays keep host launch overhead
+    # out of the per-call device time.
+    reps = max(1, args.graph_reps)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()  # first call outside capture (one-time setup)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(reps):
+                fn()
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
     times = []
     for _ in range(args.steps):
         s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s_.record()
-        fn()
+        graph.replay()
         e_.record()
         times.append((s_, e_))
     torch.cuda.synchronize()
     fg.check()
-    ms = [a.elapsed_time(b) for a, b in times]
+    ms = [a.elapsed_time(b) / reps for a, b in times]
     med = statistics.median(ms)
     out = {"case": args.case, "shape": dims, "ms_median": round(med, 5), "ms_min": round(min(ms), 5),
-           "bytes": int(nbytes), "GB/s": round(nbytes / (med * 1e-3) / 1e9, 1)}
+           "bytes": int(nbytes), "GB/s": round(nbytes / (med * 1e-3) / 1e9, 1), "graph_reps": reps}
     if work is not None:
         out["TFLOP/s"] = round(work / (med * 1e-3) / 1e12, 1)
     print(json.dumps(out), flush=True)
@@ -490,6 +506,7 @@ def main():
     ap.add_argument("--case", choices=["gemm", "quant1x128", "quant128x128", "requant"], default=None,
                     help="time a single kernel on --shape instead of the full step")
     ap.add_argument("--shape", default="4096,7168,7168")
+    ap.add_argument("--graph-reps", type=int, default=10, help="calls per captured graph in --case mode")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)

@@ -177,7 +177,14 @@ def fp8_requant_128x1(src, s_src=None, valid_rows=None, pow2=False, stream=None)
 
 # ---------------------------------------------------------------- GEMMs
 def gemm_workspace_size(M: int, N: int, K: int) -> int:
+    """Split-K workspace bytes for a dense GEMM on the current device (0: none)."""
     return int(lib.fp8fg_gemm_workspace_size(M, N, K))
+
+
+def gemm_workspace(M: int, N: int, K: int, device="cuda"):
+    """A zero-filled workspace tensor for fp8_gemm_dense_out, or None if not needed."""
+    nbytes = gemm_workspace_size(M, N, K)
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device) if nbytes else None
 
 
 def fp8_gemm_dense_out(a, sa, b, sb, c, b_scale_kind=SCALE_BLOCK128, accumulate=False, workspace=None,
@@ -199,7 +206,7 @@ def fp8_gemm_dense(a, sa, b, sb, out_dtype=torch.bfloat16, b_scale_kind=SCALE_BL
     ws = None
     nbytes = gemm_workspace_size(M, N, K)
     if nbytes:
-        ws = torch.empty(nbytes, dtype=torch.uint8, device=a.device)
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=a.device)  # counters start at zero
     return fp8_gemm_dense_out(a, sa, b, sb, c, b_scale_kind, False, ws, stream)
 
 
@@ -239,7 +246,7 @@ def fp8_gemm_grouped_masked(a, sa, b, sb, masked_m, out_dtype=torch.bfloat16, b_
 __all__ = [
     "lib", "LIB_PATH", "Fp8fgError", "scale_ld", "version", "check", "debug_set",
     "fp8_quant_1x128", "fp8_quant_1x128_out", "fp8_quant_128x128", "fp8_quant_128x128_out",
-    "fp8_requant_128x1", "fp8_requant_128x1_out", "gemm_workspace_size",
+    "fp8_requant_128x1", "fp8_requant_128x1_out", "gemm_workspace_size", "gemm_workspace",
     "fp8_gemm_dense", "fp8_gemm_dense_out", "fp8_gemm_grouped_contig", "fp8_gemm_grouped_contig_out",
     "fp8_gemm_grouped_masked", "fp8_gemm_grouped_masked_out",
 ]

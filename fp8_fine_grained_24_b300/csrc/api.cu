@@ -193,17 +193,16 @@ int fp8_requant_128x1(const void* src, int src_dtype, const float* s_src, int64_
 }
 
 size_t fp8fg_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
-  (void)M;
-  (void)N;
-  (void)K;
-  return 0;
+  if (M <= 0 || N <= 0 || K <= 0 || K % 128 != 0) return 0;
+  int err = FP8FG_OK;
+  const DeviceState* st = device_state(&err);
+  if (!st) return 0;
+  return fp8fg::gemm_workspace_bytes(fp8fg::kModeDense, M, N, K, 1, st->num_sms);
 }
 
 int fp8_gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, int b_scale_kind, void* C,
                    int out_dtype, int accumulate, int64_t M, int64_t N, int64_t K, void* workspace,
                    size_t workspace_bytes, fp8fg_stream_t stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   if (M == 0 || N == 0) {
     if (M < 0 || N < 0 || K < 0) return fail(FP8FG_ERR_INVALID_ARG, "negative size");
     return FP8FG_OK;
@@ -216,6 +215,10 @@ int fp8_gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const fl
   p.b_row = b_scale_kind == FP8FG_SCALE_ROW;
   p.C = C; p.out_f32 = out_dtype == FP8FG_FP32; p.accumulate = accumulate;
   p.rows = M; p.N = N; p.K = K; p.groups = 1; p.groupsB = 1;
+  if (workspace != nullptr && !aligned16(workspace))
+    return fail(FP8FG_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+  p.workspace = workspace;
+  p.workspace_bytes = workspace ? workspace_bytes : 0;
   return run_gemm(p, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -242,6 +242,39 @@ __device__ __forceinline__ float tile_scale(float amax, bool pow2) {
   return s;
 }
 
+// Correctly rounded x / s for a tile scale s, without a division per element.
+// r = RN(1/s) once per tile; per element q0 = RN(x*r), then two residual
+// corrections q <- RN(q + RN(x - s*q)*r) with the residual exact by FMA.
+// After the first correction q is within one ulp of x/s, and Markstein's
+// theorem (a correctly rounded reciprocal plus a within-one-ulp quotient
+// gives a correctly rounded corrected quotient) makes the second one equal
+// to RN(x/s). The sign is copied from x so that zeros keep their sign.
+// The residuals stay exact while |x| >= 2^-103; a tile whose scale is below
+// 2^-80 can hold such x with a non-negligible quotient, so it takes the
+// IEEE division instead (uniform per tile, so no divergence in practice).
+struct TileDiv {
+  float s, r;
+  bool exact;
+};
+
+__device__ __forceinline__ TileDiv make_tile_div(float s) {
+  TileDiv d;
+  d.s = s;
+  d.r = __frcp_rn(s);
+  d.exact = s < 0x1p-80f;
+  return d;
+}
+
+__device__ __forceinline__ float tile_quot(float x, const TileDiv& d) {
+  if (d.exact) return __fdiv_rn(x, d.s);
+  float q = __fmul_rn(x, d.r);
+  float e = __fmaf_rn(-d.s, q, x);
+  q = __fmaf_rn(e, d.r, q);
+  e = __fmaf_rn(-d.s, q, x);
+  q = __fmaf_rn(e, d.r, q);
+  return copysignf(q, x);
+}
+
 // Two floats -> two E4M3 bytes (RNE, satfinite); x in the low byte.
 __device__ __forceinline__ uint16_t e4m3x2(float x, float y) {
   return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(x, y), __NV_SATFINITE, __NV_E4M3));

@@ -29,6 +29,7 @@
 // the promotion warps; the shared-memory ring lets TMA run S blocks ahead.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdlib>
 #include <mutex>
 
@@ -91,16 +92,25 @@ struct KArgs {
   uint32_t* status;
   uint64_t wait_limit_ns;
   int debug_skip_fill;
+  // split-K (dense only): work item i covers tile i % num_tiles and K-split
+  // i / num_tiles; FP32 partials go to ws_partial[split][row][col] and the
+  // last of the `splits` arrivals per (tile, epilogue warp) reduces them.
+  int splits, num_items;
+  float* ws_partial;
+  int* ws_count;
 };
 
 struct Tile {
-  int gA, gB, gC, m0, n0, kbc;
+  int gA, gB, gC, m0, n0, kb0, kbc, tile, split;
   bool skip;
 };
 
-template <int BN>
-__device__ __forceinline__ Tile decode_tile(const KArgs& a, int t) {
+template <int BN, bool kSplit>
+__device__ __forceinline__ Tile decode_tile(const KArgs& a, int item) {
   Tile ti;
+  const int t = kSplit ? item % a.num_tiles : item;
+  ti.tile = t;
+  ti.split = kSplit ? item / a.num_tiles : 0;
   const int per_group = a.tiles_m * a.tiles_n;
   const int g = t / per_group;
   const int r = t - g * per_group;
@@ -108,7 +118,14 @@ __device__ __forceinline__ Tile decode_tile(const KArgs& a, int t) {
   const int nb = r / a.tiles_m;
   ti.m0 = mb * BM;
   ti.n0 = nb * BN;
-  ti.kbc = a.K / BK;
+  const int KB = a.K / BK;
+  if constexpr (kSplit) {
+    ti.kb0 = static_cast<int>(static_cast<int64_t>(KB) * ti.split / a.splits);
+    ti.kbc = static_cast<int>(static_cast<int64_t>(KB) * (ti.split + 1) / a.splits) - ti.kb0;
+  } else {
+    ti.kb0 = 0;
+    ti.kbc = KB;
+  }
   ti.skip = false;
   ti.gA = ti.gB = ti.gC = 0;
   if (a.mode == kModeContig) {
@@ -168,6 +185,50 @@ __device__ __forceinline__ void store_row(const KArgs& a, const Tile& ti, int ro
   }
 }
 
+// Split-K: store this split's FP32 partials, count the arrival of this
+// (tile, epilogue warp) and, in the warp that arrives last, replace acc by
+// the sum of all splits' partials in split order (deterministic). Returns
+// true in the warp that must store the final result. The counter is reset
+// to 0 by that warp, so the workspace stays zeroed between calls.
+// Partials are kept in the threads' own register order: slot
+// [split][tile][warp][j/4][lane] of float4, so every store and load of a
+// warp is one contiguous 512-byte access.
+template <int NC, int EW>
+__device__ __forceinline__ bool reduce_splits(const KArgs& a, const Tile& ti, int row_in_tile, int ew, int lane,
+                                              float (&acc)[NC]) {
+  const bool row_ok = ti.m0 + row_in_tile < a.rows;
+  const int64_t per_split = static_cast<int64_t>(a.num_tiles) * EW * (NC / 4) * 32;  // float4 units
+  const int64_t my_off = (static_cast<int64_t>(ti.tile) * EW + ew) * (NC / 4) * 32 + lane;
+  float4* ws4 = reinterpret_cast<float4*>(a.ws_partial);
+  if (row_ok) {
+    float4* mine = ws4 + ti.split * per_split + my_off;
+#pragma unroll
+    for (int j = 0; j < NC; j += 4) __stcg(mine + (j / 4) * 32, make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]));
+  }
+  __threadfence();
+  __syncwarp();
+  int* counter = a.ws_count + static_cast<int64_t>(ti.tile) * 16 + ew;
+  int prev = 0;
+  if (lane == 0) prev = atomicAdd(counter, 1);
+  prev = __shfl_sync(0xffffffffu, prev, 0);
+  if (prev != a.splits - 1) return false;
+  __threadfence();
+  if (lane == 0) *counter = 0;
+#pragma unroll
+  for (int j = 0; j < NC; ++j) acc[j] = 0.0f;
+  if (row_ok) {
+    for (int sp = 0; sp < a.splits; ++sp) {
+      const float4* src = ws4 + sp * per_split + my_off;
+#pragma unroll
+      for (int j = 0; j < NC; j += 4) {
+        const float4 v = __ldcg(src + (j / 4) * 32);
+        acc[j] += v.x; acc[j + 1] += v.y; acc[j + 2] += v.z; acc[j + 3] += v.w;
+      }
+    }
+  }
+  return true;
+}
+
 // acc[j] += partial[j] * sc  (block-scaled B)   or
 // acc[j] += partial[j] * sbv[j] * sa            (per-row B scales)
 template <int W, bool kBRow>
@@ -181,7 +242,7 @@ __device__ __forceinline__ void promote(float* acc, const uint32_t (&r)[W], floa
   }
 }
 
-template <int BN, bool kBRow, bool kF32>
+template <int BN, bool kBRow, bool kF32, bool kSplit>
 __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
@@ -234,10 +295,10 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       constexpr uint32_t tx = C::kABytes + C::kBBytes + C::kSABytes + (kBRow ? C::kSBBytes : 0);
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < a.num_tiles && ok; t += gridDim.x) {
-        const Tile ti = decode_tile<BN>(a, t);
+      for (int t = blockIdx.x; t < a.num_items && ok; t += gridDim.x) {
+        const Tile ti = decode_tile<BN, kSplit>(a, t);
         if (ti.skip) continue;
-        for (int kb = 0; kb < ti.kbc; ++kb, ++it) {
+        for (int kb = ti.kb0; kb < ti.kb0 + ti.kbc; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1;
           if (!mbar_wait(empty_bar(s), ph ^ 1, a.status, kStatusTimeoutProducer, a.wait_limit_ns)) {
             ok = false;
@@ -265,10 +326,10 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       constexpr uint32_t idesc = f8_idesc(BM, BN);
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < a.num_tiles && ok; t += gridDim.x) {
-        const Tile ti = decode_tile<BN>(a, t);
+      for (int t = blockIdx.x; t < a.num_items && ok; t += gridDim.x) {
+        const Tile ti = decode_tile<BN, kSplit>(a, t);
         if (ti.skip) continue;
-        for (int kb = 0; kb < ti.kbc; ++kb, ++it) {
+        for (int kb = ti.kb0; kb < ti.kb0 + ti.kbc; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1;
           const uint32_t buf = it % NB, tph = (it / NB) & 1;
           if (!mbar_wait(tempty_bar(buf), tph ^ 1, a.status, kStatusTimeoutMma, a.wait_limit_ns) ||
@@ -310,22 +371,22 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     float acc[NC];
     uint32_t it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < a.num_tiles && ok; t += gridDim.x) {
-      const Tile ti = decode_tile<BN>(a, t);
+    for (int t = blockIdx.x; t < a.num_items && ok; t += gridDim.x) {
+      const Tile ti = decode_tile<BN, kSplit>(a, t);
       if (ti.skip) continue;
 #pragma unroll
       for (int j = 0; j < NC; ++j) acc[j] = 0.0f;
-      for (int kb = 0; kb < ti.kbc; ++kb, ++it) {
+      for (int kb = ti.kb0; kb < ti.kb0 + ti.kbc; ++kb, ++it) {
         const uint32_t s = it % S, ph = (it / S) & 1;
         const uint32_t buf = it % NB, tph = (it / NB) & 1;
-        if (!kBRow && (kb % C::kSbwChunk) == 0) {
+        if (!kBRow && ((kb - ti.kb0) % C::kSbwChunk) == 0) {
           const int nbk = (ti.n0 + col0) / 128;
           const float* src = a.sB + (static_cast<int64_t>(ti.gB) * a.sb_nblk + nbk) * a.sb_kblk;
           __syncwarp();
 #pragma unroll
           for (int i = 0; i < C::kSbwChunk / 32; ++i) {
             const int k = kb + i * 32 + lane;
-            sbw[i * 32 + lane] = (nbk < a.sb_nblk && k < ti.kbc) ? __ldg(src + k) : 0.0f;
+            sbw[i * 32 + lane] = (nbk < a.sb_nblk && k < ti.kb0 + ti.kbc) ? __ldg(src + k) : 0.0f;
           }
           __syncwarp();
         }
@@ -337,7 +398,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         }
         const float sa = smem_sa[s * BM + row_in_tile];
         float sc = 0.0f;
-        if constexpr (!kBRow) sc = sa * sbw[kb % C::kSbwChunk];
+        if constexpr (!kBRow) sc = sa * sbw[(kb - ti.kb0) % C::kSbwChunk];
         const float* sbv = smem_sb + s * BN + col0;
         const uint32_t taddr = tmem_base + lane_bits + buf * BN + col0;
         tc_fence_after();
@@ -368,6 +429,9 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         }
       }
       if (!ok) break;
+      if constexpr (kSplit) {
+        if (!reduce_splits<NC, C::kEpiWarps>(a, ti, row_in_tile, ew, lane, acc)) continue;  // not the last split
+      }
       if (!(a.accumulate && ti.kbc == 0)) store_row<NC, kF32>(a, ti, row_in_tile, col0, acc);
     }
   }
@@ -407,6 +471,44 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
 }
 
 int64_t ld4(int64_t r) { return (r + 3) / 4 * 4; }
+
+// Raise the kernel's dynamic shared-memory limit once per device (the call
+// costs tens of microseconds of host time, so it is not repeated per launch).
+template <int BN, bool kBRow, bool kF32, bool kSplit>
+cudaError_t ensure_smem_attr() {
+  static std::atomic<uint64_t> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(fp8_gemm_kernel<BN, kBRow, kF32, kSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<BN>::kSmem);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
+
+// K-splitting for dense problems with too few output tiles to occupy the
+// GPU (decode-sized M): as many splits as fit on the SMs, at least four
+// 128-K blocks each, at most 32.
+int choose_splits(int mode, int64_t rows, int64_t N, int64_t K, int64_t groups, int num_sms, int bn) {
+  if (mode != kModeDense || groups != 1) return 1;
+  const int64_t tiles = ((rows + BM - 1) / BM) * ((N + bn - 1) / bn);
+  if (tiles <= 0 || tiles * 2 > num_sms) return 1;
+  int64_t s = num_sms / tiles;
+  s = s < (K / BK) / 4 ? s : (K / BK) / 4;
+  s = s < 32 ? s : 32;
+  return s < 1 ? 1 : static_cast<int>(s);
+}
+
+// Partials of every (split, tile): BM x bn floats in thread order, then 16
+// arrival counters per tile.
+size_t split_partial_bytes(int bn, int splits, int64_t num_tiles) {
+  return static_cast<size_t>(splits) * num_tiles * BM * bn * sizeof(float);
+}
+size_t split_workspace_bytes(int bn, int splits, int64_t num_tiles) {
+  return split_partial_bytes(bn, splits, num_tiles) + static_cast<size_t>(num_tiles) * 16 * sizeof(int);
+}
 
 template <int BN>
 cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limit_ns, int debug_skip_fill,
@@ -457,17 +559,44 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
   a.status = status;
   a.wait_limit_ns = wait_limit_ns;
   a.debug_skip_fill = debug_skip_fill;
+  a.splits = 1;
+  a.ws_partial = nullptr;
+  a.ws_count = nullptr;
   if (a.num_tiles == 0) return cudaSuccess;
+  const int splits = choose_splits(p.mode, p.rows, p.N, p.K, p.groups, num_sms, BN);
+  if (splits > 1 && p.workspace != nullptr &&
+      p.workspace_bytes >= split_workspace_bytes(BN, splits, a.num_tiles)) {
+    a.splits = splits;
+    a.ws_partial = static_cast<float*>(p.workspace);
+    a.ws_count = reinterpret_cast<int*>(static_cast<char*>(p.workspace) + split_partial_bytes(BN, splits, a.num_tiles));
+  }
+  a.num_items = a.num_tiles * a.splits;
 
-  auto kernel = p.b_row ? (p.out_f32 ? fp8_gemm_kernel<BN, true, true> : fp8_gemm_kernel<BN, true, false>)
-                        : (p.out_f32 ? fp8_gemm_kernel<BN, false, true> : fp8_gemm_kernel<BN, false, false>);
-  // the attribute is per function; setting it again is cheap and thread-safe
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, KArgs);
+  KernelFn kernel = nullptr;
+  cudaError_t e = cudaSuccess;
+  const int variant = (p.b_row ? 4 : 0) + (p.out_f32 ? 2 : 0) + (a.splits > 1 ? 1 : 0);
+  switch (variant) {
+#define FP8FG_VARIANT(V, R, F, S)                          \
+  case V:                                                  \
+    kernel = fp8_gemm_kernel<BN, R, F, S>;                 \
+    e = ensure_smem_attr<BN, R, F, S>();                   \
+    break;
+    FP8FG_VARIANT(0, false, false, false)
+    FP8FG_VARIANT(1, false, false, true)
+    FP8FG_VARIANT(2, false, true, false)
+    FP8FG_VARIANT(3, false, true, true)
+    FP8FG_VARIANT(4, true, false, false)
+    FP8FG_VARIANT(5, true, false, true)
+    FP8FG_VARIANT(6, true, true, false)
+    FP8FG_VARIANT(7, true, true, true)
+#undef FP8FG_VARIANT
+  }
   if (e != cudaSuccess) {
     *detail = "cudaFuncSetAttribute(max dynamic shared memory) failed";
     return e;
   }
-  const int grid = a.num_tiles < num_sms ? a.num_tiles : num_sms;
+  const int grid = a.num_items < num_sms ? a.num_items : num_sms;
   kernel<<<grid, C::kThreads, C::kSmem, stream>>>(tmA, tmB, tmSA, tmSB, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) *detail = "GEMM kernel launch failed";
@@ -488,6 +617,14 @@ int pick_bn(const GemmProblem& p) {
 }
 
 }  // namespace
+
+size_t gemm_workspace_bytes(int mode, int64_t rows, int64_t N, int64_t K, int64_t groups, int num_sms) {
+  const int bn = pick_bn(GemmProblem{});
+  const int splits = choose_splits(mode, rows, N, K, groups, num_sms, bn);
+  if (splits <= 1) return 0;
+  const int64_t tiles = ((rows + BM - 1) / BM) * ((N + bn - 1) / bn);
+  return split_workspace_bytes(bn, splits, tiles);
+}
 
 cudaError_t launch_gemm(const GemmProblem& p, uint32_t* status, uint64_t wait_limit_ns, int debug_skip_fill,
                         int num_sms, cudaStream_t stream, const char** detail) {

@@ -37,7 +37,12 @@ struct GemmProblem {
   int64_t groupsB;       // groups of B (contig: E; masked: E; dense: 1)
   const int32_t* m_indices;
   const int32_t* masked;
+  void* workspace;          // split-K scratch (zeroed before first use), or nullptr
+  size_t workspace_bytes;
 };
+
+// Bytes of split-K workspace launch_gemm uses for this problem (0: no split).
+size_t gemm_workspace_bytes(int mode, int64_t rows, int64_t N, int64_t K, int64_t groups, int num_sms);
 
 // Enqueue the GEMM. `status` is a device word that receives timeout codes.
 // Returns cudaSuccess or the first CUDA error; *detail gets a static message.

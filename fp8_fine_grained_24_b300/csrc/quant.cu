@@ -4,7 +4,10 @@
 //   requant_128x1 1x128 -> 128x1 retile for the backward pass, written
 //                 transposed (channel-major).
 // All three stream HBM once: 16-byte vector loads and stores, warp-shuffle
-// amax reductions, IEEE division for the scale and the quotient.
+// amax reductions, an IEEE division for each tile's scale and a correctly
+// rounded quotient x/s per element (tile_quot).
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -14,21 +17,43 @@ namespace {
 
 constexpr int kTile = 128;
 
-// Load 8 consecutive input elements as floats.
+// Eight consecutive input elements kept in their storage format (BF16
+// stays packed: 4 registers per 8 values) until they are needed as floats.
 template <bool kF32>
-__device__ __forceinline__ void load8(const void* p, float (&v)[8]) {
-  if constexpr (kF32) {
-    const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
-    const float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-  } else {
-    const uint4 w = __ldcs(reinterpret_cast<const uint4*>(p));
+struct Raw8;
+
+template <>
+struct Raw8<false> {
+  uint4 w;
+  __device__ __forceinline__ void load(const void* p) { w = __ldcs(reinterpret_cast<const uint4*>(p)); }
+  __device__ __forceinline__ void zero() { w = make_uint4(0, 0, 0, 0); }
+  __device__ __forceinline__ void get(float (&v)[8]) const {
     v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x);
     v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
     v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z);
     v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
   }
+};
+
+template <>
+struct Raw8<true> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const void* p) {
+    a = __ldcs(reinterpret_cast<const float4*>(p));
+    b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+  }
+  __device__ __forceinline__ void zero() { a = b = make_float4(0.f, 0.f, 0.f, 0.f); }
+  __device__ __forceinline__ void get(float (&v)[8]) const {
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+};
+
+template <bool kF32>
+__device__ __forceinline__ void load8(const void* p, float (&v)[8]) {
+  Raw8<kF32> r;
+  r.load(p);
+  r.get(v);
 }
 
 __device__ __forceinline__ float amax8(const float (&v)[8]) {
@@ -38,67 +63,82 @@ __device__ __forceinline__ float amax8(const float (&v)[8]) {
   return a;
 }
 
-__device__ __forceinline__ uint2 quant8(const float (&v)[8], float s) {
+template <bool kF32>
+__device__ __forceinline__ float amax8(const Raw8<kF32>& r) {
+  float v[8];
+  r.get(v);
+  return amax8(v);
+}
+
+__device__ __forceinline__ uint2 quant8(const float (&v)[8], const TileDiv& d) {
   uint32_t w[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float a = __fdiv_rn(v[2 * i], s);
-    const float b = __fdiv_rn(v[2 * i + 1], s);
-    w[i] = e4m3x2(a, b);
-  }
+  for (int i = 0; i < 4; ++i) w[i] = e4m3x2(tile_quot(v[2 * i], d), tile_quot(v[2 * i + 1], d));
   return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
 }
 
+template <bool kF32>
+__device__ __forceinline__ uint2 quant8(const Raw8<kF32>& r, const TileDiv& d) {
+  float v[8];
+  r.get(v);
+  return quant8(v, d);
+}
+
 // ------------------------------------------------------------ 1x128
-// A half-warp owns one 1x128 tile: 16 lanes x 8 elements. Tiles are visited
-// row-major (row m, K-block kb), so consecutive half-warps read consecutive
-// 256/512-byte segments of a row.
+// A half-warp owns one 1x128 tile: 16 lanes x 8 elements. A warp's work unit
+// is one row and a run of 2*kUnroll consecutive tiles of it (the two
+// half-warps take alternate tiles), so each thread keeps kUnroll 16-byte
+// loads in flight and consecutive half-warps read consecutive 256/512-byte
+// segments of the row. Units are visited row-major; one 32-bit division per
+// unit (the launcher checks that the unit count fits 32 bits).
 template <bool kF32, int kUnroll>
 __global__ void __launch_bounds__(256) quant_1x128_kernel(const void* __restrict__ x, int64_t ldx,
                                                           int64_t M, int64_t K, uint8_t* __restrict__ q,
                                                           float* __restrict__ s, int64_t lds, int pow2) {
-  const int64_t KB = K / kTile;
-  const int64_t tiles = M * KB;
+  constexpr int kRun = 2 * kUnroll;
+  const uint32_t KB = static_cast<uint32_t>(K / kTile);
+  const uint32_t runs_per_row = (KB + kRun - 1) / kRun;
+  const uint32_t units = static_cast<uint32_t>(M) * runs_per_row;
   const int lane = threadIdx.x & 31;
   const int j = lane & 15;  // 8-element chunk within the tile
-  const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t warps_total = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int half = lane >> 4;
+  const uint32_t warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint32_t warps_total = (gridDim.x * blockDim.x) >> 5;
   const size_t esz = kF32 ? 4 : 2;
 
-  for (int64_t base = warp_global * 2 * kUnroll; base < tiles; base += warps_total * 2 * kUnroll) {
-    float v[kUnroll][8];
-    int64_t tile[kUnroll];
+  for (uint32_t unit = warp_global; unit < units; unit += warps_total) {
+    const uint32_t m = unit / runs_per_row;
+    const uint32_t kb0 = (unit - m * runs_per_row) * kRun;
+    const char* xrow = static_cast<const char*>(x) + (static_cast<int64_t>(m) * ldx + j * 8) * esz;
+    Raw8<kF32> v[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      tile[u] = base + 2 * u + (lane >> 4);
-      if (tile[u] < tiles) {
-        const int64_t m = tile[u] / KB, kb = tile[u] - m * KB;
-        const char* p = static_cast<const char*>(x) + (m * ldx + kb * kTile + j * 8) * esz;
-        load8<kF32>(p, v[u]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[u][i] = 0.0f;
-      }
+      const uint32_t kb = kb0 + 2 * u + half;
+      if (kb < KB)
+        v[u].load(xrow + static_cast<int64_t>(kb) * kTile * esz);
+      else
+        v[u].zero();
     }
+    uint8_t* qrow = q + static_cast<int64_t>(m) * K + j * 8;
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t kb = kb0 + 2 * u + half;
       float a = amax8(v[u]);
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
       const float sc = tile_scale(a, pow2 != 0);
-      if (tile[u] < tiles) {
-        const int64_t m = tile[u] / KB, kb = tile[u] - m * KB;
-        const uint2 packed = quant8(v[u], sc);
-        *reinterpret_cast<uint2*>(q + m * K + kb * kTile + j * 8) = packed;
-        if (j == 0) s[kb * lds + m] = sc;
+      if (kb < KB) {
+        *reinterpret_cast<uint2*>(qrow + static_cast<int64_t>(kb) * kTile) = quant8(v[u], make_tile_div(sc));
+        if (j == 0) s[static_cast<int64_t>(kb) * lds + m] = sc;
       }
     }
   }
 }
 
 // ------------------------------------------------------------ 128x128
-// One CTA (256 threads) per 128x128 block. Warp w covers rows w*16 .. w*16+15,
-// two rows per load instruction (16 lanes x 16 bytes per bf16 row).
+// One CTA (256 threads) per 128x128 block, held in registers in storage
+// format (BF16: 32 registers per thread). Warp w covers rows w*16 .. w*16+15,
+// two rows per load instruction (16 lanes x 16 bytes per BF16 row).
 template <bool kF32>
 __global__ void __launch_bounds__(256) quant_128x128_kernel(const void* __restrict__ w, int64_t N, int64_t K,
                                                             uint8_t* __restrict__ q, float* __restrict__ s,
@@ -115,19 +155,18 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const void* __restri
   const char* wg = static_cast<const char*>(w) + g * N * K * esz;
 
   constexpr int kRowsPerThread = 8;
-  float v[kRowsPerThread][8];
-  float a = 0.0f;
+  Raw8<kF32> v[kRowsPerThread];
 #pragma unroll
   for (int i = 0; i < kRowsPerThread; ++i) {
     const int64_t row = nb * kTile + warp * 16 + i * 2 + (lane >> 4);
-    if (row < N) {
-      load8<kF32>(wg + (row * K + kb * kTile + chunk * 8) * esz, v[i]);
-    } else {
-#pragma unroll
-      for (int t = 0; t < 8; ++t) v[i][t] = 0.0f;
-    }
-    a = fmaxf(a, amax8(v[i]));
+    if (row < N)
+      v[i].load(wg + (row * K + kb * kTile + chunk * 8) * esz);
+    else
+      v[i].zero();
   }
+  float a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kRowsPerThread; ++i) a = fmaxf(a, amax8(v[i]));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
   __shared__ float red[8];
@@ -137,12 +176,13 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const void* __restri
 #pragma unroll
   for (int i = 1; i < 8; ++i) a = fmaxf(a, red[i]);
   const float sc = tile_scale(a, pow2 != 0);
+  const TileDiv d = make_tile_div(sc);
   uint8_t* qg = q + g * N * K;
 #pragma unroll
   for (int i = 0; i < kRowsPerThread; ++i) {
     const int64_t row = nb * kTile + warp * 16 + i * 2 + (lane >> 4);
     if (row < N) {
-      *reinterpret_cast<uint2*>(qg + row * K + kb * kTile + chunk * 8) = quant8(v[i], sc);
+      *reinterpret_cast<uint2*>(qg + row * K + kb * kTile + chunk * 8) = quant8(v[i], d);
     }
   }
   if (threadIdx.x == 0) s[(g * NB + nb) * KB + kb] = sc;
@@ -245,13 +285,13 @@ __global__ void __launch_bounds__(256) requant_128x1_kernel(const void* __restri
     const int idx = tid + i * 256;  // 1024 = 128 channels x 8 token chunks
     const int c = (idx & 31) + ((idx >> 8) << 5);
     const int t16 = (idx >> 5) & 7;
-    const float sc = part[c];
+    const TileDiv d = make_tile_div(part[c]);
     uint32_t w[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       const float* col = xs + (t16 * 16 + b * 4) * kRqStride + c;
-      const uint32_t lo = e4m3x2(__fdiv_rn(col[0], sc), __fdiv_rn(col[kRqStride], sc));
-      const uint32_t hi = e4m3x2(__fdiv_rn(col[2 * kRqStride], sc), __fdiv_rn(col[3 * kRqStride], sc));
+      const uint32_t lo = e4m3x2(tile_quot(col[0], d), tile_quot(col[kRqStride], d));
+      const uint32_t hi = e4m3x2(tile_quot(col[2 * kRqStride], d), tile_quot(col[3 * kRqStride], d));
       w[b] = lo | (hi << 16);
     }
     *reinterpret_cast<uint4*>(qg + (cb * kTile + c) * T + tb * kTile + t16 * 16) =
@@ -267,14 +307,29 @@ int grid_for(int64_t work_items, int per_block_items, int num_sms, int blocks_pe
   return static_cast<int>(want);
 }
 
+// Raise the requantizer's dynamic shared-memory limit once per device.
+template <int kSrc>
+cudaError_t ensure_requant_attr() {
+  static std::atomic<uint64_t> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(requant_128x1_kernel<kSrc>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRqSmem);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
+
 }  // namespace
 
 cudaError_t launch_quant_1x128(const void* x, bool f32, int64_t M, int64_t K, int64_t ldx, uint8_t* q, float* s,
                                int64_t lds, int pow2, int num_sms, cudaStream_t stream) {
-  constexpr int kUnroll = 2;
-  const int64_t tiles = M * (K / kTile);
-  // 256 threads = 8 warps = 16 tiles per pass per block (x kUnroll)
-  const int grid = grid_for(tiles, 16 * kUnroll, num_sms, 8);
+  constexpr int kUnroll = 4;
+  const int64_t runs = M * ((K / kTile + 2 * kUnroll - 1) / (2 * kUnroll));
+  if (runs >= (1ll << 32) || M >= (1ll << 32)) return cudaErrorInvalidValue;
+  // 256 threads = 8 warps = 8 work units per pass per block
+  const int grid = grid_for(runs, 8, num_sms, 8);
   if (f32)
     quant_1x128_kernel<true, kUnroll><<<grid, 256, 0, stream>>>(x, ldx, M, K, q, s, lds, pow2);
   else
@@ -302,17 +357,17 @@ cudaError_t launch_requant_128x1(const void* src, int src_kind, const float* s_s
   cudaError_t e = cudaSuccess;
   switch (src_kind) {
     case 0:
-      e = cudaFuncSetAttribute(requant_128x1_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRqSmem);
+      e = ensure_requant_attr<0>();
       if (e != cudaSuccess) return e;
       requant_128x1_kernel<0><<<grid, 256, kRqSmem, stream>>>(src, s_src, ld_t, T, C, valid_rows, qT, sT, ld_c, pow2);
       break;
     case 1:
-      e = cudaFuncSetAttribute(requant_128x1_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRqSmem);
+      e = ensure_requant_attr<1>();
       if (e != cudaSuccess) return e;
       requant_128x1_kernel<1><<<grid, 256, kRqSmem, stream>>>(src, s_src, ld_t, T, C, valid_rows, qT, sT, ld_c, pow2);
       break;
     default:
-      e = cudaFuncSetAttribute(requant_128x1_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRqSmem);
+      e = ensure_requant_attr<2>();
       if (e != cudaSuccess) return e;
       requant_128x1_kernel<2><<<grid, 256, kRqSmem, stream>>>(src, s_src, ld_t, T, C, valid_rows, qT, sT, ld_c, pow2);
       break;

@@ -144,10 +144,13 @@ FP8FG_API int fp8_requant_128x1(const void* src, int src_dtype, const float* s_s
  *   C          [M][N] of out_dtype (BF16 or FP32), written
  *   accumulate 1: C += result (FP32 output only: weight-gradient
  *              accumulation); 0: C = result
- *   workspace  device scratch of at least fp8fg_gemm_workspace_size(M, N, K)
- *              bytes, 16-byte aligned (may be NULL when that size is 0);
- *              its contents need no initialisation and are left in a state
- *              that the next call reuses.
+ *   workspace  device scratch for splitting K when M is too small to occupy
+ *              the GPU (decode): fp8fg_gemm_workspace_size(M, N, K) bytes,
+ *              16-byte aligned, zero-filled before its first use; every call
+ *              leaves it zero-filled again (re-zero it after a call that
+ *              reported FP8FG_ERR_TIMEOUT). Calls that share a workspace must
+ *              not overlap on the GPU. NULL, or fewer bytes than that size,
+ *              runs the same product without splitting K.
  * Requires K % 128 == 0, N % 8 == 0, 16-byte aligned A, B, C.
  */
 FP8FG_API int fp8_gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
@@ -155,7 +158,8 @@ FP8FG_API int fp8_gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B
                    int64_t M, int64_t N, int64_t K,
                    void* workspace, size_t workspace_bytes, fp8fg_stream_t stream);
 
-/* Bytes of workspace fp8_gemm_dense needs for this shape (0 if none). */
+/* Bytes of workspace fp8_gemm_dense uses for this shape on the current
+ * device (0 if it does not split K). Needs a CUDA device; 0 on error. */
 FP8FG_API size_t fp8fg_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /*

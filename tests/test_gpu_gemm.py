@@ -281,3 +281,72 @@ def test_timeout_reports_error_and_context_survives(lib):
     c = lib.fp8_gemm_dense(qa_d, sa_d, qb_d, sb_d)
     lib.check()
     compare_gemm(c, gemm.gemm_dense(qa, sa, qb, sb), True)
+
+
+# ---------------------------------------------------------------- split-K (decode-sized M)
+def _split_case(fg, M, N, K, seed, out_dtype=torch.bfloat16, accumulate=False):
+    x = wl.activations(M, K, seed, device="cpu")
+    w = wl.weights((N, K), seed + 1, device="cpu")
+    qa, sa, qa_d, sa_d = _quant_a(x)
+    qb, sb, qb_d, sb_d = _quant_b(w)
+    ws = fg.gemm_workspace(M, N, K)
+    assert ws is not None, "expected a K-split for this shape"
+    cref = gemm.gemm_dense(qa, sa, qb, sb)
+    base = torch.randn((M, N), dtype=torch.float32, device="cuda") if accumulate else None
+    for _ in range(2):  # the workspace counters must come back to zero
+        c = base.clone() if accumulate else torch.empty((M, N), dtype=out_dtype, device="cuda")
+        fg.fp8_gemm_dense_out(qa_d, sa_d, qb_d, sb_d, c, accumulate=accumulate, workspace=ws)
+        torch.cuda.synchronize()
+        ref = cref + base.double().cpu().numpy() if accumulate else cref
+        compare_gemm(c, ref, out_dtype == torch.bfloat16)
+    return ws
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 2048), (64, 512, 4096), (130, 264, 2048), (128, 1024, 7168)])
+def test_split_k_matches_oracle(lib, M, N, K):
+    _split_case(lib, M, N, K, seed=M + N)
+
+
+def test_split_k_fp32_accumulate(lib):
+    _split_case(lib, 64, 520, 2048, seed=81, out_dtype=torch.float32, accumulate=True)
+
+
+def test_split_k_small_workspace_falls_back(lib):
+    M, N, K = 64, 512, 2048
+    x = wl.activations(M, K, 82, device="cpu")
+    w = wl.weights((N, K), 83, device="cpu")
+    qa, sa, qa_d, sa_d = _quant_a(x)
+    qb, sb, qb_d, sb_d = _quant_b(w)
+    small = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    lib.fp8_gemm_dense_out(qa_d, sa_d, qb_d, sb_d, c, workspace=small)
+    compare_gemm(c, gemm.gemm_dense(qa, sa, qb, sb), True)
+    assert torch.count_nonzero(small) == 0
+
+
+def test_split_k_wgrad_row_scales(lib):
+    # weight gradient with many tokens and a small output: K (tokens) is split
+    T, N, C = 2048, 136, 264
+    qgT, sgT, qxT, sxT = _wgrad_operands(T, N, C, 84)
+    ws = lib.gemm_workspace(N, C, T)
+    assert ws is not None
+    out = torch.empty((N, C), dtype=torch.float32, device="cuda")
+    lib.fp8_gemm_dense_out(dev(qgT), dev(pad_rows_scale(sgT, N)), dev(qxT), dev(pad_rows_scale(sxT, C)), out,
+                           b_scale_kind=lib.SCALE_ROW, workspace=ws)
+    compare_gemm(out, gemm.wgrad(qgT, sgT, qxT, sxT), False)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("M,N,K", wl.DECODE_CASES)
+def test_decode_full_sampled(lib, M, N, K):
+    x = wl.activations(M, K, 1003, device="cuda")
+    w = wl.weights((N, K), 1004 + N, device="cuda")
+    qa_d, sa_d = lib.fp8_quant_1x128(x)
+    qb_d, sb_d = lib.fp8_quant_128x128(w)
+    c = lib.fp8_gemm_dense(qa_d, sa_d, qb_d, sb_d)
+    torch.cuda.synchronize()
+    qa, sa = quant.quant_1x128(to_np32(x))
+    for nb in (0, 13, N // 128 - 1):
+        cols = slice(nb * 128, nb * 128 + 128)
+        qb, sb = quant.quant_128x128(to_np32(w[cols]))
+        compare_gemm(c[:, cols], gemm.gemm_dense(qa, sa, qb, sb), True)
