@@ -123,6 +123,10 @@ int run_gemm(const fp8fg::GemmProblem& p, cudaStream_t stream) {
 
 }  // namespace
 
+namespace fp8fg {
+void set_last_error(const char* msg) { t_last_error = msg; }
+}  // namespace fp8fg
+
 extern "C" {
 
 int64_t fp8fg_scale_ld(int64_t rows) { return rows <= 0 ? 0 : (rows + 3) / 4 * 4; }

@@ -626,6 +626,18 @@ size_t gemm_workspace_bytes(int mode, int64_t rows, int64_t N, int64_t K, int64_
   return split_workspace_bytes(bn, splits, tiles);
 }
 
+void gemm_workspace_zero_range(int mode, int64_t rows, int64_t N, int64_t K, int64_t groups, int num_sms,
+                               size_t* offset, size_t* bytes) {
+  const int bn = pick_bn(GemmProblem{});
+  const int splits = choose_splits(mode, rows, N, K, groups, num_sms, bn);
+  *offset = 0;
+  *bytes = 0;
+  if (splits <= 1) return;
+  const int64_t tiles = ((rows + BM - 1) / BM) * ((N + bn - 1) / bn);
+  *offset = split_partial_bytes(bn, splits, tiles);
+  *bytes = split_workspace_bytes(bn, splits, tiles) - *offset;
+}
+
 cudaError_t launch_gemm(const GemmProblem& p, uint32_t* status, uint64_t wait_limit_ns, int debug_skip_fill,
                         int num_sms, cudaStream_t stream, const char** detail) {
   switch (pick_bn(p)) {

@@ -44,6 +44,14 @@ struct GemmProblem {
 // Bytes of split-K workspace launch_gemm uses for this problem (0: no split).
 size_t gemm_workspace_bytes(int mode, int64_t rows, int64_t N, int64_t K, int64_t groups, int num_sms);
 
+// Record the calling thread's last error message (fp8fg_last_error_string).
+void set_last_error(const char* msg);
+
+// Byte range of that workspace that must be zero when a launch starts (the
+// split-arrival counters); *bytes = 0 when the problem does not split.
+void gemm_workspace_zero_range(int mode, int64_t rows, int64_t N, int64_t K, int64_t groups, int num_sms,
+                               size_t* offset, size_t* bytes);
+
 // Enqueue the GEMM. `status` is a device word that receives timeout codes.
 // Returns cudaSuccess or the first CUDA error; *detail gets a static message.
 cudaError_t launch_gemm(const GemmProblem& p, uint32_t* status, uint64_t wait_limit_ns, int debug_skip_fill,

@@ -158,6 +158,27 @@ FP8FG_API int fp8_gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B
                    int64_t M, int64_t N, int64_t K,
                    void* workspace, size_t workspace_bytes, fp8fg_stream_t stream);
 
+/*
+ * fp8_gemm_dense_noalloc -- fp8_gemm_dense for callers that cannot allocate
+ * device memory. (No counterpart in the paper: a deployment convenience of
+ * this library.) Some callers only receive device pointers from a host
+ * application that owns all device memory and offers no allocator, or run
+ * where a device allocation is forbidden; they cannot provide the split-K
+ * workspace. This entry point computes the same product with the same
+ * arguments minus the workspace, using instead a 24 MiB array that the
+ * library reserves in device memory when it is loaded (on every GPU the
+ * process uses, until exit). It allocates nothing.
+ *   - The first call on a device looks up that array's device address;
+ *     that first call should come before any stream capture.
+ *   - All calls share the array: calls whose GPU work overlaps race on it.
+ *   - Each call clears the part of the array that must start at zero.
+ *   - A shape needing more scratch than 24 MiB is rejected with
+ *     FP8FG_ERR_UNSUPPORTED_SHAPE (none exists on GPUs with up to ~190 SMs).
+ */
+FP8FG_API int fp8_gemm_dense_noalloc(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                                     int b_scale_kind, void* C, int out_dtype, int accumulate,
+                                     int64_t M, int64_t N, int64_t K, fp8fg_stream_t stream);
+
 /* Bytes of workspace fp8_gemm_dense uses for this shape on the current
  * device (0 if it does not split K). Needs a CUDA device; 0 on error. */
 FP8FG_API size_t fp8fg_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
