@@ -6,26 +6,52 @@ CUDA kernels. The functions carry the names of the C entry points declared
 in ``include/fp8fg.h``; the ``*_out`` variants write into caller-provided
 tensors and allocate nothing.
 
-Importing this package loads the shared library and fails loudly
-(ImportError) if it has not been built: there is no fallback path.
-Build it with ``python -m fp8_fine_grained_24_b300.build``.
+The shared library is loaded on first use (so that the ``build`` submodule
+can be imported before it exists); any call without the built library
+raises ImportError: there is no fallback path. Build it with
+``python -m fp8_fine_grained_24_b300.build``.
 """
 from __future__ import annotations
 
 import ctypes
 import os
+import threading
 
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8fg.so")
 
-if not os.path.exists(LIB_PATH):
-    raise ImportError(
-        f"{LIB_PATH} is missing: build it with `python -m fp8_fine_grained_24_b300.build` "
-        "(nvcc, sm_103a). The library has no non-CUDA fallback.")
 
-lib = ctypes.CDLL(LIB_PATH)
+class _Library:
+    """ctypes handle of libfp8fg.so, opened (and typed) on first attribute access."""
+
+    def __init__(self):
+        self._cdll = None
+        self._lock = threading.Lock()
+
+    def _open(self):
+        with self._lock:
+            if self._cdll is None:
+                if not os.path.exists(LIB_PATH):
+                    raise ImportError(
+                        f"{LIB_PATH} is missing: build it with `python -m fp8_fine_grained_24_b300.build` "
+                        "(nvcc, sm_103a). The library has no non-CUDA fallback.")
+                cdll = ctypes.CDLL(LIB_PATH)
+                for name, (res, args) in _SIGS.items():
+                    f = getattr(cdll, name)
+                    f.restype = res
+                    f.argtypes = args
+                self._cdll = cdll
+        return self._cdll
+
+    def __getattr__(self, name):
+        if name.startswith("_"):
+            raise AttributeError(name)
+        return getattr(self._cdll if self._cdll is not None else self._open(), name)
+
+
+lib = _Library()
 
 # ---------------------------------------------------------------- constants
 OK = 0
@@ -61,11 +87,9 @@ _SIGS = {
     "fp8fg_last_error_string": (ctypes.c_char_p, []),
     "fp8fg_version": (ctypes.c_char_p, []),
     "fp8fg_debug_set": (_c_int, [_c_int, _c_i64]),
+    "fp8_gemm_dense_noalloc": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_int, _c_int, _c_i64, _c_i64,
+                                        _c_i64, _c_vp]),
 }
-for _name, (_res, _args) in _SIGS.items():
-    _f = getattr(lib, _name)
-    _f.restype = _res
-    _f.argtypes = _args
 
 
 class Fp8fgError(RuntimeError):
