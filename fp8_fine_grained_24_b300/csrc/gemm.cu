@@ -274,7 +274,10 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     if (kBRow) prefetch_tmap(&tmSB);
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1 + C::kEpiWarps);
+      // a stage is free once every promotion warp has seen its K block's MMAs
+      // complete (tmem_full) and has read its scales: the MMA issuer does not
+      // need to commit to it, which keeps its per-block loop short
+      mbar_init(empty_bar(s), C::kEpiWarps);
     }
     for (int b = 0; b < NB; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -346,7 +349,6 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
             // advance 32 bytes (= 32 E4M3 elements) along K inside the swizzle atom
             mma_f8f6f4(d, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
           }
-          mma_commit(empty_bar(s));
           mma_commit(tfull_bar(buf));
         }
       }
