@@ -35,6 +35,7 @@ if ROOT not in sys.path:
 M_PREFILL, K_PREFILL = 4096, 7168
 N_PREFILL = (2112, 24576, 7168, 4096)
 METRIC = "FP8 block-scaled GEMM TFLOP/s & % of B300 FP8 peak; quant GB/s vs HBM"
+L2_ROTATE_BYTES = 3 * 126 * 2**20  # --case mode: working set of consecutive calls
 FP8_PER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor rate ratio (4.5 / 2.25 PFLOP/s)
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
@@ -443,43 +444,57 @@ def run_case(args):
 
     dims = [int(v) for v in args.shape.split(",")]
     dev = torch.device("cuda", 0)
-    if args.case == "gemm":
-        M, N, K = dims
-        qa, sa = fg.fp8_quant_1x128(wl.activations(M, K, 1001, device=dev))
-        qb, sb = fg.fp8_quant_128x128(wl.weights((N, K), 1002, device=dev))
-        c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        ws = fg.gemm_workspace(M, N, K, device=dev)
-        fn = lambda: fg.fp8_gemm_dense_out(qa, sa, qb, sb, c, workspace=ws)  # noqa: E731
-        work, unit, nbytes = gemm_flops(M, N, K), "TFLOP/s", gemm_bytes(M, N, K)
-    elif args.case == "quant1x128":
-        M, K = dims
-        x = wl.activations(M, K, 1001, device=dev)
-        q = torch.empty((M, K), dtype=torch.uint8, device=dev)
-        s = torch.empty((K // 128, fg.scale_ld(M)), dtype=torch.float32, device=dev)
-        fn = lambda: fg.fp8_quant_1x128_out(x, q, s)  # noqa: E731
-        work, unit, nbytes = None, "GB/s", quant_1x128_bytes(M, K)
-    elif args.case == "quant128x128":
-        N, K = dims
-        w = wl.weights((N, K), 1002, device=dev)
-        q = torch.empty((N, K), dtype=torch.uint8, device=dev)
-        s = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=dev)
-        fn = lambda: fg.fp8_quant_128x128_out(w, q, s)  # noqa: E731
-        work, unit, nbytes = None, "GB/s", quant_128x128_bytes(N, K)
-    elif args.case == "requant":
-        T, C = dims
-        qa, sa = fg.fp8_quant_1x128(wl.activations(T, C, 1001, device=dev))
-        qT = torch.empty((C, T), dtype=torch.uint8, device=dev)
-        sT = torch.empty((T // 128, fg.scale_ld(C)), dtype=torch.float32, device=dev)
-        fn = lambda: fg.fp8_requant_128x1_out(qa.view(torch.float8_e4m3fn), sa, qT, sT, pow2=True)  # noqa: E731
-        work, unit, nbytes = None, "GB/s", T * C * 2 + T * (C // 128) * 4 + (T // 128) * C * 4
-    else:
+
+    def make(seed):
+        """One independent buffer set: returns (call, algorithmic bytes, flops or None)."""
+        if args.case == "gemm":
+            M, N, K = dims
+            qa, sa = fg.fp8_quant_1x128(wl.activations(M, K, seed, device=dev))
+            qb, sb = fg.fp8_quant_128x128(wl.weights((N, K), seed + 1, device=dev))
+            c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ws = fg.gemm_workspace(M, N, K, device=dev)
+            return (lambda: fg.fp8_gemm_dense_out(qa, sa, qb, sb, c, workspace=ws),
+                    gemm_bytes(M, N, K), gemm_flops(M, N, K))
+        if args.case == "quant1x128":
+            M, K = dims
+            x = wl.activations(M, K, seed, device=dev)
+            q = torch.empty((M, K), dtype=torch.uint8, device=dev)
+            s = torch.empty((K // 128, fg.scale_ld(M)), dtype=torch.float32, device=dev)
+            return lambda: fg.fp8_quant_1x128_out(x, q, s), quant_1x128_bytes(M, K), None
+        if args.case == "quant128x128":
+            N, K = dims
+            w = wl.weights((N, K), seed + 1, device=dev)
+            q = torch.empty((N, K), dtype=torch.uint8, device=dev)
+            s = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=dev)
+            return lambda: fg.fp8_quant_128x128_out(w, q, s), quant_128x128_bytes(N, K), None
+        if args.case == "requant":
+            T, C = dims
+            qa, sa = fg.fp8_quant_1x128(wl.activations(T, C, seed, device=dev))
+            qT = torch.empty((C, T), dtype=torch.uint8, device=dev)
+            sT = torch.empty((T // 128, fg.scale_ld(C)), dtype=torch.float32, device=dev)
+            return (lambda: fg.fp8_requant_128x1_out(qa.view(torch.float8_e4m3fn), sa, qT, sT, pow2=True),
+                    T * C * 2 + T * (C // 128) * 4 + (T // 128) * C * 4, None)
         raise SystemExit(f"unknown case {args.case}")
+
+    # Independent buffer sets, called round robin, so that the working set
+    # of consecutive calls exceeds the 126 MB L2 (every call reads from HBM).
+    first = make(1001)
+    nbytes, work = first[1], first[2]
+    nsets = 1 if args.no_rotate else max(1, min(8, -(-L2_ROTATE_BYTES // max(1, nbytes))))
+    fns = [first[0]] + [make(1001 + 10 * i)[0] for i in range(1, nsets)]
+    unit = "TFLOP/s" if work is not None else "GB/s"
+    calls = [0]
+
+    def fn():
+        fns[calls[0] % nsets]()
+        calls[0] += 1
+
     for _ in range(args.warmup):
         fn()
     fg.check()
     # R calls captured in one CUDA graph: replays keep host launch overhead
     # out of the per-call device time.
-    reps = max(1, args.graph_reps)
+    reps = -(-max(1, args.graph_reps) // nsets) * nsets  # whole rounds over the buffer sets
     stream = torch.cuda.Stream()
     stream.wait_stream(torch.cuda.current_stream())
     graph = torch.cuda.CUDAGraph()
@@ -504,7 +519,8 @@ def run_case(args):
     ms = [a.elapsed_time(b) / reps for a, b in times]
     med = statistics.median(ms)
     out = {"case": args.case, "shape": dims, "ms_median": round(med, 5), "ms_min": round(min(ms), 5),
-           "bytes": int(nbytes), "GB/s": round(nbytes / (med * 1e-3) / 1e9, 1), "graph_reps": reps}
+           "bytes": int(nbytes), "GB/s": round(nbytes / (med * 1e-3) / 1e9, 1), "graph_reps": reps,
+           "buffer_sets": nsets}
     if work is not None:
         out["TFLOP/s"] = round(work / (med * 1e-3) / 1e12, 1)
     print(json.dumps(out), flush=True)
@@ -516,6 +532,8 @@ def main():
                     help="time a single kernel on --shape instead of the full step")
     ap.add_argument("--shape", default="4096,7168,7168")
     ap.add_argument("--graph-reps", type=int, default=10, help="calls per captured graph in --case mode")
+    ap.add_argument("--no-rotate", action="store_true",
+                    help="--case mode: reuse one buffer set (L2-warm when it fits in L2)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)

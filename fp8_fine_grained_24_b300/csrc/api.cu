@@ -75,6 +75,10 @@ const DeviceState* device_state(int* err) {
   return &st;
 }
 
+fp8fg::QuantLaunch quant_launch(const DeviceState* st) {
+  return fp8fg::QuantLaunch{st->num_sms, st->status, g_wait_limit_ns.load(), g_debug_skip_fill.load()};
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
@@ -152,7 +156,7 @@ int fp8_quant_1x128(const void* x, int x_dtype, int64_t M, int64_t K, int64_t ld
   const DeviceState* st = device_state(&err);
   if (!st) return err;
   cudaError_t e = fp8fg::launch_quant_1x128(x, x_dtype == FP8FG_FP32, M, K, ldx, q, s, fp8fg_scale_ld(M), pow2,
-                                            st->num_sms, reinterpret_cast<cudaStream_t>(stream));
+                                            quant_launch(st), reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FP8FG_OK : cuda_fail(e, "quant_1x128 launch");
 }
 
@@ -170,7 +174,7 @@ int fp8_quant_128x128(const void* w, int w_dtype, int64_t G, int64_t N, int64_t 
   int err = FP8FG_OK;
   const DeviceState* st = device_state(&err);
   if (!st) return err;
-  cudaError_t e = fp8fg::launch_quant_128x128(w, w_dtype == FP8FG_FP32, G, N, K, q, s, pow2,
+  cudaError_t e = fp8fg::launch_quant_128x128(w, w_dtype == FP8FG_FP32, G, N, K, q, s, pow2, quant_launch(st),
                                               reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FP8FG_OK : cuda_fail(e, "quant_128x128 launch");
 }
@@ -185,14 +189,16 @@ int fp8_requant_128x1(const void* src, int src_dtype, const float* s_src, int64_
     return fail(FP8FG_ERR_UNSUPPORTED_SHAPE, "T=%lld and C=%lld must be multiples of 128", (long long)T, (long long)C);
   if (G == 0 || T == 0 || C == 0) return FP8FG_OK;
   if (!src || !qT || !sT || (src_dtype == FP8FG_E4M3 && !s_src)) return fail(FP8FG_ERR_INVALID_ARG, "null pointer");
-  if (!aligned16(src) || !aligned16(qT) || !aligned4(sT) || (s_src && !aligned4(s_src)))
-    return fail(FP8FG_ERR_MISALIGNED, "src, qT must be 16-byte aligned, scales 4-byte aligned");
+  if (!aligned16(src) || !aligned16(qT) || !aligned4(sT) || (s_src && !aligned16(s_src)))
+    return fail(FP8FG_ERR_MISALIGNED, "src, qT and s_src must be 16-byte aligned, sT 4-byte aligned");
   if (valid_rows && !aligned4(valid_rows)) return fail(FP8FG_ERR_MISALIGNED, "valid_rows must be 4-byte aligned");
   int err = FP8FG_OK;
-  if (!device_state(&err)) return err;
+  const DeviceState* st = device_state(&err);
+  if (!st) return err;
   const int kind = src_dtype == FP8FG_E4M3 ? 0 : (src_dtype == FP8FG_BF16 ? 1 : 2);
   cudaError_t e = fp8fg::launch_requant_128x1(src, kind, s_src, fp8fg_scale_ld(T), G, T, C, valid_rows, qT, sT,
-                                              fp8fg_scale_ld(C), pow2, reinterpret_cast<cudaStream_t>(stream));
+                                              fp8fg_scale_ld(C), pow2, quant_launch(st),
+                                              reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FP8FG_OK : cuda_fail(e, "requant_128x1 launch");
 }
 

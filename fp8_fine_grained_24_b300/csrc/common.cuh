@@ -66,6 +66,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes or about `hint_ns` pass, so that a waiting warp takes almost no
+// issue slots from the warps that are working.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity. Gives up after
 // `limit_ns` of wall time (checked every 256 polls) or after 2^26 polls.
 // With a status word: also gives up as soon as another thread has recorded
@@ -87,6 +102,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
   return false;
 }
 
+// mbar_wait whose polls sleep (mbar_try_wait_sleep, 1 us hint); the limit is
+// checked every 64 polls.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, uint32_t* status, uint32_t code,
+                                                uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1; i < (1u << 26); ++i) {
+    if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
+    if ((i & 63u) == 0) {
+      if (status != nullptr && *reinterpret_cast<volatile uint32_t*>(status) != 0) return false;
+      if (globaltimer_ns() - t0 > limit_ns) break;
+    }
+  }
+  if (status != nullptr) atomicCAS(status, 0u, code);
+  return false;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -99,6 +131,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
+}
+
+// Non-tensor bulk copy of `bytes` (a multiple of 16) from global memory to
+// shared memory, completing on an mbarrier; both addresses 16-byte aligned.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -220,74 +260,6 @@ __host__ __device__ constexpr uint32_t f8_idesc(int m, int n) {
 }
 
 // ---------------------------------------------------------------- numerics
-// Scale of a tile from its amax: fl32(amax / 448) by IEEE division; 1 when
-// that is zero; optionally raised to the next power of two.
-__device__ __forceinline__ float tile_scale(float amax, bool pow2) {
-  float s = __fdiv_rn(amax, 448.0f);
-  if (!(s > 0.0f)) s = 1.0f;
-  if (pow2) {
-    uint32_t b = __float_as_uint(s);
-    uint32_t e = b >> 23;          // sign is 0: s > 0
-    uint32_t m = b & 0x7FFFFFu;
-    if (e != 0) {
-      if (m != 0) b = (e + 1) << 23;
-    } else {
-      // subnormal: value m * 2^-149; next power of two of the integer m
-      uint32_t p = 1u << (31 - __clz(m));
-      if (p != m) p <<= 1;
-      b = p;  // 2^23 lands on the smallest normal, 0x00800000
-    }
-    s = __uint_as_float(b);
-  }
-  return s;
-}
-
-// Correctly rounded x / s for a tile scale s, without a division per element.
-// r = RN(1/s) once per tile; per element q0 = RN(x*r), then two residual
-// corrections q <- RN(q + RN(x - s*q)*r) with the residual exact by FMA.
-// After the first correction q is within one ulp of x/s, and Markstein's
-// theorem (a correctly rounded reciprocal plus a within-one-ulp quotient
-// gives a correctly rounded corrected quotient) makes the second one equal
-// to RN(x/s). The sign is copied from x so that zeros keep their sign.
-// The residuals stay exact while |x| >= 2^-103; a tile whose scale is below
-// 2^-80 can hold such x with a non-negligible quotient, so it takes the
-// IEEE division instead (uniform per tile, so no divergence in practice).
-struct TileDiv {
-  float s, r;
-  bool exact;
-};
-
-__device__ __forceinline__ TileDiv make_tile_div(float s) {
-  TileDiv d;
-  d.s = s;
-  d.r = __frcp_rn(s);
-  d.exact = s < 0x1p-80f;
-  return d;
-}
-
-__device__ __forceinline__ float tile_quot(float x, const TileDiv& d) {
-  if (d.exact) return __fdiv_rn(x, d.s);
-  float q = __fmul_rn(x, d.r);
-  float e = __fmaf_rn(-d.s, q, x);
-  q = __fmaf_rn(e, d.r, q);
-  e = __fmaf_rn(-d.s, q, x);
-  q = __fmaf_rn(e, d.r, q);
-  return copysignf(q, x);
-}
-
-// Two floats -> two E4M3 bytes (RNE, satfinite); x in the low byte.
-__device__ __forceinline__ uint16_t e4m3x2(float x, float y) {
-  return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(x, y), __NV_SATFINITE, __NV_E4M3));
-}
-
-__device__ __forceinline__ float e4m3_to_f32(uint8_t v) {
-  __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(v), __NV_E4M3);
-  return __half2float(__half(h));
-}
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

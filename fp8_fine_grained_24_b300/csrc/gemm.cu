@@ -27,14 +27,12 @@
 // gridDim.x, in M-fastest order so that concurrently running CTAs share the
 // same B tiles in L2. Several TMEM buffers let the tensor core run ahead of
 // the promotion warps; the shared-memory ring lets TMA run S blocks ahead.
-#include <cudaTypedefs.h>
-
 #include <atomic>
 #include <cstdlib>
-#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tmap.h"
 
 namespace fp8fg {
 
@@ -446,32 +444,6 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
-              uint64_t stride1, uint64_t stride2, uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[3] = {d0, d1, d2};
-  const cuuint64_t strides[2] = {stride1, stride2};
-  const cuuint32_t box[3] = {b0, b1, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int64_t ld4(int64_t r) { return (r + 3) / 4 * 4; }
 
 // Raise the kernel's dynamic shared-memory limit once per device (the call

@@ -7,16 +7,26 @@
 
 namespace fp8fg {
 
+// Launch context shared by the quantizer launchers: SM count (grid size),
+// the device status word that receives timeout codes, the bounded-wait limit
+// and the test hook that makes a producer skip one of its fills (-1: off).
+struct QuantLaunch {
+  int num_sms;
+  uint32_t* status;
+  uint64_t wait_limit_ns;
+  int debug_skip_fill;
+};
+
 cudaError_t launch_quant_1x128(const void* x, bool f32, int64_t M, int64_t K, int64_t ldx, uint8_t* q, float* s,
-                               int64_t lds, int pow2, int num_sms, cudaStream_t stream);
+                               int64_t lds, int pow2, const QuantLaunch& l, cudaStream_t stream);
 
 cudaError_t launch_quant_128x128(const void* w, bool f32, int64_t G, int64_t N, int64_t K, uint8_t* q, float* s,
-                                 int pow2, cudaStream_t stream);
+                                 int pow2, const QuantLaunch& l, cudaStream_t stream);
 
 // src_kind: 0 E4M3 (+ s_src with row stride ld_t), 1 BF16, 2 FP32
 cudaError_t launch_requant_128x1(const void* src, int src_kind, const float* s_src, int64_t ld_t, int64_t G,
                                  int64_t T, int64_t C, const int32_t* valid_rows, uint8_t* qT, float* sT,
-                                 int64_t ld_c, int pow2, cudaStream_t stream);
+                                 int64_t ld_c, int pow2, const QuantLaunch& l, cudaStream_t stream);
 
 // Scheduling modes of the GEMM kernel.
 enum GemmMode : int { kModeDense = 0, kModeContig = 1, kModeMaskedRows = 2, kModeMaskedK = 3 };

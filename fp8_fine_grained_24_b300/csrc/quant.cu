@@ -1,378 +1,644 @@
-// Fine-grained E4M3 quantizers (DeepSeek-V3 report excerpt, pages 1-2):
+// Fine-grained E4M3 quantizers (DeepSeek-V3 report excerpt, "Fine-Grained
+// Quantization"; DeepGEMM article, "Fine-grained scaling"):
 //   quant_1x128   one scale per row per 128 columns (activations),
 //   quant_128x128 one scale per 128x128 block (weights),
 //   requant_128x1 1x128 -> 128x1 retile for the backward pass, written
 //                 transposed (channel-major).
-// All three stream HBM once: 16-byte vector loads and stores, warp-shuffle
-// amax reductions, an IEEE division for each tile's scale and a correctly
-// rounded quotient x/s per element (tile_quot).
+//
+// All three are the same persistent pipeline. One CTA per SM; warp 0 is a
+// TMA producer that streams the input in 16-64 KB chunks (one 128-column
+// strip of rows, one 128x128 block, one 128x128 tile) through a ring of
+// shared-memory stages; 16 consumer warps read a chunk from shared memory
+// into registers, release the stage, reduce the amax (warp shuffles, and for
+// the 2-D tiles partial maxima exchanged through shared memory behind an
+// mbarrier), then write E4M3 codes and scales straight to global memory
+// with row-contiguous stores. The ring keeps about 192 KB of loads in
+// flight per SM, so HBM streams continuously while the consumers compute.
+//
+// The consumers are bound by instruction issue, so the element arithmetic
+// is kept lean: values are unpacked already negated (free for BF16) so that
+// the correctly rounded quotient runs as five packed f32x2 operations per
+// pair (quot2_fma), chunk coordinates advance as a mixed-radix counter
+// instead of being divided out per chunk, and the quotient path (exact
+// multiply for power-of-two scales, FMA-corrected otherwise) is chosen
+// once per chunk by a warp vote.
+//
+// Every wait is bounded (see mbar_wait_sleep); a timeout is recorded in the
+// device status word and the CTA winds down after its copies have landed.
 #include <atomic>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "quant_math.cuh"
+#include "tmap.h"
 
 namespace fp8fg {
 
 namespace {
 
 constexpr int kTile = 128;
+constexpr int kConsumerWarps = 16;
+constexpr int kThreads = 32 * (1 + kConsumerWarps);
+constexpr int kRingBytes = 192 * 1024;
 
-// Eight consecutive input elements kept in their storage format (BF16
-// stays packed: 4 registers per 8 values) until they are needed as floats.
-template <bool kF32>
-struct Raw8;
+enum : uint32_t { kStatusTimeoutQuantProducer = 5, kStatusTimeoutQuantConsumer = 6, kStatusTimeoutQuantDrain = 7 };
 
-template <>
-struct Raw8<false> {
-  uint4 w;
-  __device__ __forceinline__ void load(const void* p) { w = __ldcs(reinterpret_cast<const uint4*>(p)); }
-  __device__ __forceinline__ void zero() { w = make_uint4(0, 0, 0, 0); }
-  __device__ __forceinline__ void get(float (&v)[8]) const {
-    v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x);
-    v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
-    v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z);
-    v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+struct Pipe {
+  uint32_t* status;
+  uint64_t wait_limit_ns;
+  int debug_skip_fill;
+};
+
+// Chunk coordinates (d2, d1, d0) of chunk index c = (d2 * R1 + d1) * R0 + d0,
+// advanced by a fixed step (gridDim.x) with carries instead of divisions.
+struct Walk {
+  int64_t d2;
+  int d1, d0;
+  int r1, r0;
+  int64_t s2;
+  int s1, s0;
+
+  __device__ __forceinline__ void init(int64_t c, int64_t step, int radix1, int radix0) {
+    r1 = radix1;
+    r0 = radix0;
+    const int64_t per2 = static_cast<int64_t>(r1) * r0;
+    d2 = c / per2;
+    const int64_t rem = c - d2 * per2;
+    d1 = static_cast<int>(rem / r0);
+    d0 = static_cast<int>(rem - static_cast<int64_t>(d1) * r0);
+    s2 = step / per2;
+    const int64_t srem = step - s2 * per2;
+    s1 = static_cast<int>(srem / r0);
+    s0 = static_cast<int>(srem - static_cast<int64_t>(s1) * r0);
+  }
+
+  __device__ __forceinline__ void advance() {
+    d0 += s0;
+    int carry = d0 >= r0;
+    if (carry) d0 -= r0;
+    d1 += s1 + carry;
+    carry = d1 >= r1;
+    if (carry) d1 -= r1;
+    d2 += s2 + carry;
   }
 };
 
-template <>
-struct Raw8<true> {
-  float4 a, b;
-  __device__ __forceinline__ void load(const void* p) {
-    a = __ldcs(reinterpret_cast<const float4*>(p));
-    b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
-  }
-  __device__ __forceinline__ void zero() { a = b = make_float4(0.f, 0.f, 0.f, 0.f); }
-  __device__ __forceinline__ void get(float (&v)[8]) const {
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-  }
-};
-
+// Eight consecutive elements of a row from shared memory, negated, as four
+// f32 pairs.
 template <bool kF32>
-__device__ __forceinline__ void load8(const void* p, float (&v)[8]) {
-  Raw8<kF32> r;
-  r.load(p);
-  r.get(v);
+__device__ __forceinline__ void load_neg8(const uint8_t* p, uint64_t (&v)[4]) {
+  if constexpr (kF32) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 b = *reinterpret_cast<const float4*>(p + 16);
+    v[0] = pk2(-a.x, -a.y);
+    v[1] = pk2(-a.z, -a.w);
+    v[2] = pk2(-b.x, -b.y);
+    v[3] = pk2(-b.z, -b.w);
+  } else {
+    const uint4 w = *reinterpret_cast<const uint4*>(p);
+    v[0] = neg_bf16x2(w.x);
+    v[1] = neg_bf16x2(w.y);
+    v[2] = neg_bf16x2(w.z);
+    v[3] = neg_bf16x2(w.w);
+  }
 }
 
-__device__ __forceinline__ float amax8(const float (&v)[8]) {
-  float a = fabsf(v[0]);
+__device__ __forceinline__ float amax4pk(const uint64_t (&v)[4]) {
+  float a = 0.0f;
 #pragma unroll
-  for (int i = 1; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
+  for (int i = 0; i < 4; ++i) a = amax_pk(v[i], a);
   return a;
 }
 
-template <bool kF32>
-__device__ __forceinline__ float amax8(const Raw8<kF32>& r) {
-  float v[8];
-  r.get(v);
-  return amax8(v);
+__device__ __forceinline__ uint2 codes8(const uint64_t (&v)[4]) {
+  return make_uint2(e4m3x4_pk(v[0], v[1]), e4m3x4_pk(v[2], v[3]));
 }
 
-__device__ __forceinline__ uint2 quant8(const float (&v)[8], const TileDiv& d) {
-  uint32_t w[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) w[i] = e4m3x2(tile_quot(v[2 * i], d), tile_quot(v[2 * i + 1], d));
-  return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+// ---------------------------------------------------------------- pipeline
+// Shared memory: kStages stages of kStageBytes, then full[S], empty[S] and
+// one exchange barrier (8 bytes each), then the exchange buffer.
+template <class Op>
+struct Layout {
+  static constexpr int kBarOff = Op::kStages * Op::kStageBytes;
+  static constexpr int kRedOff = (kBarOff + (2 * Op::kStages + 1) * 8 + 15) / 16 * 16;
+  static constexpr int kSmem = kRedOff + Op::kRedBytes;
+};
+
+// Per-chunk context handed to a consumer.
+struct Slot {
+  const uint8_t* st;  // the stage's shared memory
+  uint32_t full, empty, ph;
+  uint32_t red_bar;
+  float* red;
+  uint32_t it;  // this CTA's chunk counter (exchange-buffer parity)
+};
+
+// Warp 0 lane 0 fills stages; warps 1..16 consume them in the same chunk
+// order (chunk c = blockIdx.x + i * gridDim.x).
+template <class Op>
+__global__ void __launch_bounds__(kThreads, 1)
+    quant_pipe_kernel(const __grid_constant__ CUtensorMap tm, const typename Op::Args a, const Pipe p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  constexpr int S = Op::kStages;
+  using L = Layout<Op>;
+  const uint32_t base = smem_u32(smem);
+  const uint32_t bar0 = base + L::kBarOff;
+  const uint32_t red_bar = bar0 + 2 * S * 8;
+  float* red = reinterpret_cast<float*>(smem + L::kRedOff);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t chunks = a.chunks;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar0 + s * 8, 1);
+      mbar_init(bar0 + (S + s) * 8, kConsumerWarps);
+    }
+    mbar_init(red_bar, kConsumerWarps);
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  Walk w;
+  Op::walk_init(a, w, blockIdx.x, gridDim.x);
+  uint32_t it = 0, s = 0, ph = 0;
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tm);
+      for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x, ++it, w.advance()) {
+        if (!mbar_wait_sleep(bar0 + (S + s) * 8, ph ^ 1, p.status, kStatusTimeoutQuantProducer, p.wait_limit_ns))
+          break;
+        if (static_cast<int>(it) != p.debug_skip_fill)  // test hook: a fill that never lands
+          Op::issue(tm, a, w, base + s * Op::kStageBytes, bar0 + s * 8);
+        if (++s == S) {
+          s = 0;
+          ph ^= 1;
+        }
+      }
+      // No copy may still be landing in shared memory when the CTA exits:
+      // wait (bounded, ignoring the error word) for the last fill of each stage.
+      const uint32_t first = it > static_cast<uint32_t>(S) ? it - S : 0;
+      for (uint32_t i = first; i < it; ++i) {
+        if (static_cast<int>(i) == p.debug_skip_fill) continue;
+        if (!mbar_wait_sleep(bar0 + (i % S) * 8, (i / S) & 1, nullptr, 0, p.wait_limit_ns))
+          atomicCAS(p.status, 0u, kStatusTimeoutQuantDrain);
+      }
+    }
+    return;
+  }
+
+  const int cw = warp - 1;
+  for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x, ++it, w.advance()) {
+    const Slot sl{smem + s * Op::kStageBytes, bar0 + s * 8, bar0 + (S + s) * 8, ph, red_bar, red, it};
+    if (!Op::consume(a, p, w, sl, cw, lane)) break;
+    if (++s == S) {
+      s = 0;
+      ph ^= 1;
+    }
+  }
 }
 
-template <bool kF32>
-__device__ __forceinline__ uint2 quant8(const Raw8<kF32>& r, const TileDiv& d) {
-  float v[8];
-  r.get(v);
-  return quant8(v, d);
+__device__ __forceinline__ bool wait_full(const Slot& sl, const Pipe& p) {
+  return mbar_wait_sleep(sl.full, sl.ph, p.status, kStatusTimeoutQuantConsumer, p.wait_limit_ns);
+}
+
+// Release a stage once the whole warp has read it into registers. The
+// reads went through the generic proxy and the producer's next fill writes
+// through the async (TMA) proxy, which the mbarrier handshake alone does not
+// order: without the proxy fence a read still in flight could see the next
+// chunk (observed on FP32 inputs). Callers also release only after the
+// loaded values have been consumed (the amax reduction), so the fence has
+// nothing left to wait for.
+__device__ __forceinline__ void release(const Slot& sl, int lane) {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+  if (lane == 0) mbar_arrive(sl.empty);
+}
+
+// Post this warp's partial maxima (written before the call) and wait until
+// all 16 consumer warps have posted theirs for this chunk.
+__device__ __forceinline__ bool exchange(const Slot& sl, const Pipe& p, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(sl.red_bar);
+  return mbar_wait_sleep(sl.red_bar, sl.it & 1, p.status, kStatusTimeoutQuantConsumer, p.wait_limit_ns);
 }
 
 // ------------------------------------------------------------ 1x128
-// A half-warp owns one 1x128 tile: 16 lanes x 8 elements. A warp's work unit
-// is one row and a run of 2*kUnroll consecutive tiles of it (the two
-// half-warps take alternate tiles), so each thread keeps kUnroll 16-byte
-// loads in flight and consecutive half-warps read consecutive 256/512-byte
-// segments of the row. Units are visited row-major; one 32-bit division per
-// unit (the launcher checks that the unit count fits 32 bits).
-template <bool kF32, int kUnroll>
-__global__ void __launch_bounds__(256) quant_1x128_kernel(const void* __restrict__ x, int64_t ldx,
-                                                          int64_t M, int64_t K, uint8_t* __restrict__ q,
-                                                          float* __restrict__ s, int64_t lds, int pow2) {
-  constexpr int kRun = 2 * kUnroll;
-  const uint32_t KB = static_cast<uint32_t>(K / kTile);
-  const uint32_t runs_per_row = (KB + kRun - 1) / kRun;
-  const uint32_t units = static_cast<uint32_t>(M) * runs_per_row;
-  const int lane = threadIdx.x & 31;
-  const int j = lane & 15;  // 8-element chunk within the tile
-  const int half = lane >> 4;
-  const uint32_t warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const uint32_t warps_total = (gridDim.x * blockDim.x) >> 5;
-  const size_t esz = kF32 ? 4 : 2;
+// Chunk: rows [rb*R, rb*R + R) x columns [kb*128, kb*128 + 128), R = 128
+// (BF16) or 64 (FP32), one 32 KB TMA box; kb runs fastest. Consumer warp w
+// takes 2*I rows (I = R/32); each half-warp one row per step (16 lanes x 8
+// elements), so a warp reads 2 rows per shared-memory instruction and writes
+// two 128-byte row segments of q. The scalar work of a tile (the division
+// by 448, the reciprocal) is done once per tile rather than on each of its
+// 16 lanes: the warp's 2*I row maxima are gathered one per lane, every lane
+// computes one scale, and each step fetches its tile's scale by shuffle.
+template <bool kF32>
+struct Quant1x128 {
+  static constexpr int kEsz = kF32 ? 4 : 2;
+  static constexpr int kRows = kF32 ? 64 : 128;
+  static constexpr int kStageBytes = kRows * kTile * kEsz;
+  static constexpr int kStages = kRingBytes / kStageBytes;
+  static constexpr int kRedBytes = 0;
+  static constexpr int kIters = kRows / kConsumerWarps / 2;  // 4 (BF16) or 2 (FP32)
+  static constexpr int kWarpRows = 2 * kIters;
 
-  for (uint32_t unit = warp_global; unit < units; unit += warps_total) {
-    const uint32_t m = unit / runs_per_row;
-    const uint32_t kb0 = (unit - m * runs_per_row) * kRun;
-    const char* xrow = static_cast<const char*>(x) + (static_cast<int64_t>(m) * ldx + j * 8) * esz;
-    Raw8<kF32> v[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const uint32_t kb = kb0 + 2 * u + half;
-      if (kb < KB)
-        v[u].load(xrow + static_cast<int64_t>(kb) * kTile * esz);
-      else
-        v[u].zero();
-    }
-    uint8_t* qrow = q + static_cast<int64_t>(m) * K + j * 8;
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const uint32_t kb = kb0 + 2 * u + half;
-      float a = amax8(v[u]);
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-      const float sc = tile_scale(a, pow2 != 0);
-      if (kb < KB) {
-        *reinterpret_cast<uint2*>(qrow + static_cast<int64_t>(kb) * kTile) = quant8(v[u], make_tile_div(sc));
-        if (j == 0) s[static_cast<int64_t>(kb) * lds + m] = sc;
-      }
-    }
+  struct Args {
+    int64_t chunks, M, K, lds;
+    int KB;
+    uint8_t* q;
+    float* s;
+    int pow2;
+  };
+
+  // d2 = row block, d0 = 128-column block
+  static __device__ __forceinline__ void walk_init(const Args& a, Walk& w, int64_t c, int64_t step) {
+    w.init(c, step, 1, a.KB);
   }
-}
+
+  static __device__ __forceinline__ void issue(const CUtensorMap& tm, const Args&, const Walk& w, uint32_t dst,
+                                               uint32_t full) {
+    mbar_arrive_expect_tx(full, kStageBytes);
+    tma_load_3d(dst, &tm, full, w.d0 * kTile, static_cast<int32_t>(w.d2 * kRows), 0);
+  }
+
+  static __device__ __forceinline__ bool consume(const Args& a, const Pipe& p, const Walk& w, const Slot& sl,
+                                                 int cw, int lane) {
+    const int half = lane >> 4, j = lane & 15;
+    if (!wait_full(sl, p)) return false;
+    uint64_t v[kIters][4];
+#pragma unroll
+    for (int i = 0; i < kIters; ++i)
+      load_neg8<kF32>(sl.st + ((cw * kWarpRows + 2 * i + half) * kTile + j * 8) * kEsz, v[i]);
+    // row maxima: after the xor-shuffles every lane of half h holds am[i] of row 2i+h
+    float am[kIters];
+#pragma unroll
+    for (int i = 0; i < kIters; ++i) {
+      am[i] = amax4pk(v[i]);
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) am[i] = fmaxf(am[i], __shfl_xor_sync(0xffffffffu, am[i], o));
+    }
+    release(sl, lane);
+    // lane L takes row t = L % (2I): am[t/2] of half t%2
+    const int t = lane & (kWarpRows - 1);
+    float my_am = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kIters; ++i) {
+      const float x = __shfl_sync(0xffffffffu, am[i], 16 * (t & 1));
+      if ((t >> 1) == i) my_am = x;
+    }
+    const float my_s = tile_scale(my_am, a.pow2 != 0);
+    const float my_r = __frcp_rn(my_s);
+    const int path = warp_quot_mode(make_tile_div_mode(my_s));
+    const int64_t row0 = w.d2 * kRows + cw * kWarpRows;
+    const int64_t col = static_cast<int64_t>(w.d0) * kTile;
+    if (lane < kWarpRows && row0 + lane < a.M) a.s[w.d0 * a.lds + row0 + lane] = my_s;
+    uint8_t* qp = a.q + (row0 + half) * a.K + col + j * 8;
+    const int64_t rows_left = a.M - row0 - half;
+#pragma unroll
+    for (int i = 0; i < kIters; ++i) {
+      const float sc = __shfl_sync(0xffffffffu, my_s, 2 * i + half);
+      const float rc = __shfl_sync(0xffffffffu, my_r, 2 * i + half);
+      quot2_n<4>(v[i], path, sc, rc);
+      if (2 * i < rows_left) *reinterpret_cast<uint2*>(qp) = codes8(v[i]);
+      qp += 2 * a.K;
+    }
+    return true;
+  }
+};
 
 // ------------------------------------------------------------ 128x128
-// One CTA (256 threads) per 128x128 block, held in registers in storage
-// format (BF16: 32 registers per thread). Warp w covers rows w*16 .. w*16+15,
-// two rows per load instruction (16 lanes x 16 bytes per BF16 row).
+// Chunk: one 128x128 block (32 KB BF16 box; FP32 as two 64-row boxes),
+// k blocks fastest. Consumer warp w holds rows 8w .. 8w+7 in registers
+// (half-warp per row), reduces its amax, posts it to the exchange buffer and
+// arrives on the exchange barrier; after the barrier every warp has the
+// block's amax. The buffer is double-buffered by chunk parity: a warp can
+// only be one chunk ahead of the slowest, because the barrier needs all 16
+// arrivals.
 template <bool kF32>
-__global__ void __launch_bounds__(256) quant_128x128_kernel(const void* __restrict__ w, int64_t N, int64_t K,
-                                                            uint8_t* __restrict__ q, float* __restrict__ s,
-                                                            int pow2) {
-  const int64_t KB = K / kTile;
-  const int64_t NB = (N + kTile - 1) / kTile;
-  const int64_t blk = blockIdx.x;
-  const int64_t g = blk / (NB * KB);
-  const int64_t r = blk - g * NB * KB;
-  const int64_t nb = r / KB, kb = r - (r / KB) * KB;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int chunk = lane & 15;
-  const size_t esz = kF32 ? 4 : 2;
-  const char* wg = static_cast<const char*>(w) + g * N * K * esz;
+struct Quant128x128 {
+  static constexpr int kEsz = kF32 ? 4 : 2;
+  static constexpr int kStageBytes = kTile * kTile * kEsz;
+  static constexpr int kBoxRows = kF32 ? 64 : 128;
+  static constexpr int kStages = kRingBytes / kStageBytes;
+  static constexpr int kRedBytes = 2 * kConsumerWarps * 4;
+  static constexpr int kIters = kTile / kConsumerWarps / 2;
 
-  constexpr int kRowsPerThread = 8;
-  Raw8<kF32> v[kRowsPerThread];
-#pragma unroll
-  for (int i = 0; i < kRowsPerThread; ++i) {
-    const int64_t row = nb * kTile + warp * 16 + i * 2 + (lane >> 4);
-    if (row < N)
-      v[i].load(wg + (row * K + kb * kTile + chunk * 8) * esz);
-    else
-      v[i].zero();
+  struct Args {
+    int64_t chunks, N, K;
+    int NB, KB;
+    uint8_t* q;
+    float* s;
+    int pow2;
+  };
+
+  // d2 = group, d1 = 128-row block, d0 = 128-column block
+  static __device__ __forceinline__ void walk_init(const Args& a, Walk& w, int64_t c, int64_t step) {
+    w.init(c, step, a.NB, a.KB);
   }
-  float a = 0.0f;
+
+  static __device__ __forceinline__ void issue(const CUtensorMap& tm, const Args&, const Walk& w, uint32_t dst,
+                                               uint32_t full) {
+    mbar_arrive_expect_tx(full, kStageBytes);
 #pragma unroll
-  for (int i = 0; i < kRowsPerThread; ++i) a = fmaxf(a, amax8(v[i]));
+    for (int i = 0; i < kTile / kBoxRows; ++i)
+      tma_load_3d(dst + i * kBoxRows * kTile * kEsz, &tm, full, w.d0 * kTile, w.d1 * kTile + i * kBoxRows,
+                  static_cast<int32_t>(w.d2));
+  }
+
+  static __device__ __forceinline__ bool consume(const Args& a, const Pipe& p, const Walk& w, const Slot& sl,
+                                                 int cw, int lane) {
+    const int half = lane >> 4, j = lane & 15;
+    if (!wait_full(sl, p)) return false;
+    uint64_t v[kIters][4];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-  __shared__ float red[8];
-  if (lane == 0) red[warp] = a;
-  __syncthreads();
-  a = red[0];
+    for (int i = 0; i < kIters; ++i)
+      load_neg8<kF32>(sl.st + ((cw * (2 * kIters) + 2 * i + half) * kTile + j * 8) * kEsz, v[i]);
+    float am = 0.0f;
 #pragma unroll
-  for (int i = 1; i < 8; ++i) a = fmaxf(a, red[i]);
-  const float sc = tile_scale(a, pow2 != 0);
-  const TileDiv d = make_tile_div(sc);
-  uint8_t* qg = q + g * N * K;
+    for (int i = 0; i < kIters; ++i) am = fmaxf(am, amax4pk(v[i]));
 #pragma unroll
-  for (int i = 0; i < kRowsPerThread; ++i) {
-    const int64_t row = nb * kTile + warp * 16 + i * 2 + (lane >> 4);
-    if (row < N) {
-      *reinterpret_cast<uint2*>(qg + row * K + kb * kTile + chunk * 8) = quant8(v[i], d);
+    for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    release(sl, lane);
+    float* rb = sl.red + (sl.it & 1) * kConsumerWarps;
+    if (lane == 0) rb[cw] = am;
+    if (!exchange(sl, p, lane)) return false;
+    const float4* r4 = reinterpret_cast<const float4*>(rb);
+#pragma unroll
+    for (int i = 0; i < kConsumerWarps / 4; ++i) {
+      const float4 t = r4[i];
+      am = fmaxf(am, fmaxf(fmaxf(t.x, t.y), fmaxf(t.z, t.w)));
     }
+    const float sc = tile_scale(am, a.pow2 != 0);
+    const float rc = __frcp_rn(sc);
+    const int path = make_tile_div_mode(sc);  // the same block scale in every lane
+    const int row_in = w.d1 * kTile + cw * (2 * kIters) + half;
+    uint8_t* qp = a.q + (w.d2 * a.N + row_in) * a.K + static_cast<int64_t>(w.d0) * kTile + j * 8;
+    const int64_t rows_left = a.N - row_in;
+#pragma unroll
+    for (int i = 0; i < kIters; ++i) {
+      quot2_n<4>(v[i], path, sc, rc);
+      if (2 * i < rows_left) *reinterpret_cast<uint2*>(qp) = codes8(v[i]);
+      qp += 2 * a.K;
+    }
+    if (cw == 0 && lane == 0) a.s[(w.d2 * a.NB + w.d1) * a.KB + w.d0] = sc;
+    return true;
   }
-  if (threadIdx.x == 0) s[(g * NB + nb) * KB + kb] = sc;
-}
+};
 
 // ------------------------------------------------------------ 128x1
-// One CTA per (group, 128-token block, 128-channel block). The source tile
-// is dequantized into shared memory as FP32 [token][channel] (row stride 129
-// floats: column reads are bank-conflict free), per-channel amax over the
-// 128 tokens gives the 128x1 scales, and each output row (one channel, 128
-// tokens) is written as eight 16-byte stores.
-constexpr int kRqStride = kTile + 1;
-constexpr int kRqSmem = kTile * kRqStride * 4 + 2 * kTile * 4;
-
+// Chunk: one 128-token x 128-channel source tile (E4M3 16 KB, BF16 32 KB,
+// FP32 two 64-token boxes), token blocks fastest so that consecutive chunks
+// extend the same output rows. Consumer warp w takes tokens 16*(w%8) .. +15
+// of channels 64*(w/8) .. +63, two adjacent channels per lane: per token one
+// shared-memory read covers 64 contiguous channels. Per-channel partial
+// maxima over the 16 tokens go to the exchange buffer [parity][8][128]; after
+// the barrier each lane reduces the 8 partials of its channels, computes the
+// 128x1 scales and writes each channel's 16 codes as one 16-byte store into
+// the transposed output row. A tile wholly at or beyond the group's valid
+// rows is not loaded: it quantizes to zeros with scale 1.
 template <int kSrc>  // 0: E4M3 + 1x128 scales, 1: BF16, 2: FP32
-__global__ void __launch_bounds__(256) requant_128x1_kernel(const void* __restrict__ src,
-                                                            const float* __restrict__ s_src, int64_t ld_t,
-                                                            int64_t T, int64_t C,
-                                                            const int32_t* __restrict__ valid_rows,
-                                                            uint8_t* __restrict__ qT, float* __restrict__ sT,
-                                                            int64_t ld_c, int pow2) {
-  extern __shared__ float rq_smem[];
-  float* xs = rq_smem;                      // [128][129]
-  float* part = rq_smem + kTile * kRqStride;  // [2][128]
-  const int64_t TB = T / kTile, CB = C / kTile;
-  const int64_t blk = blockIdx.x;
-  const int64_t g = blk / (TB * CB);
-  const int64_t r = blk - g * TB * CB;
-  const int64_t tb = r / CB, cb = r - (r / CB) * CB;
-  const int tid = threadIdx.x;
-  const int64_t valid = valid_rows ? static_cast<int64_t>(valid_rows[g]) : T;
+struct Requant128x1 {
+  static constexpr int kEsz = kSrc == 0 ? 1 : (kSrc == 1 ? 2 : 4);
+  static constexpr int kTileBytes = kTile * kTile * kEsz;
+  // an E4M3 tile carries its 128 token scales (512 B) behind it
+  static constexpr int kStageBytes = kTileBytes + (kSrc == 0 ? kTile * 4 : 0);
+  static constexpr int kBoxRows = kSrc == 2 ? 64 : 128;
+  static constexpr int kStages = kRingBytes / kStageBytes;
+  static constexpr int kRedBytes = 2 * 8 * kTile * 4;
+  // rows past the valid count are +0; stored negated that is (-0, -0)
+  static constexpr uint64_t kNegZero2 = 0x8000000080000000ull;
 
-  // ---- load + dequantize
-  if constexpr (kSrc == 0) {
-    const uint8_t* sp = static_cast<const uint8_t*>(src) + g * T * C;
-    const float* ss = s_src + g * CB * ld_t + cb * ld_t;  // ss[t]: scale of token t, channel block cb
+  struct Args {
+    int64_t chunks, T, C, ld_t, ld_c;
+    int TB, CB;
+    const float* s_src;
+    const int32_t* valid_rows;
+    uint8_t* qT;
+    float* sT;
+    int pow2;
+  };
+
+  // d2 = group, d1 = 128-channel block, d0 = 128-token block
+  static __device__ __forceinline__ void walk_init(const Args& a, Walk& w, int64_t c, int64_t step) {
+    w.init(c, step, a.CB, a.TB);
+  }
+
+  static __device__ __forceinline__ int64_t valid_of(const Args& a, int64_t g) {
+    return a.valid_rows ? static_cast<int64_t>(__ldg(a.valid_rows + g)) : a.T;
+  }
+
+  static __device__ __forceinline__ void issue(const CUtensorMap& tm, const Args& a, const Walk& w, uint32_t dst,
+                                               uint32_t full) {
+    if (static_cast<int64_t>(w.d0) * kTile >= valid_of(a, w.d2)) {
+      mbar_arrive(full);  // nothing to load: the consumers write zeros
+      return;
+    }
+    mbar_arrive_expect_tx(full, kStageBytes);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int idx = tid + i * 256;      // 1024 chunks of 16 bytes
-      const int t = idx >> 3, c16 = idx & 7;
-      const int64_t tok = tb * kTile + t;
-      float* dst = xs + t * kRqStride + c16 * 16;
-      if (tok < valid) {
-        const uint4 w = __ldcs(reinterpret_cast<const uint4*>(sp + tok * C + cb * kTile + c16 * 16));
-        const float sc = ss[tok];
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    for (int i = 0; i < kTile / kBoxRows; ++i)
+      tma_load_3d(dst + i * kBoxRows * kTile * kEsz, &tm, full, w.d1 * kTile, w.d0 * kTile + i * kBoxRows,
+                  static_cast<int32_t>(w.d2));
+    if constexpr (kSrc == 0)
+      bulk_load(dst + kTileBytes, a.s_src + (w.d2 * a.CB + w.d1) * a.ld_t + static_cast<int64_t>(w.d0) * kTile,
+                kTile * 4, full);
+  }
+
+  static __device__ __forceinline__ bool consume(const Args& a, const Pipe& p, const Walk& w, const Slot& sl,
+                                                 int cw, int lane) {
+    const int64_t g = w.d2;
+    const int tg = cw & 7, chh = cw >> 3;
+    const int c0 = chh * 64 + 2 * lane;  // this lane's first channel within the tile
+    const int64_t tile_t0 = static_cast<int64_t>(w.d0) * kTile;
+    const int64_t t0 = tile_t0 + tg * 16;
+    const int64_t valid = valid_of(a, g);
+    const bool live = tile_t0 < valid;  // the tile has at least one valid row
+    if (!wait_full(sl, p)) return false;
+
+    // x[k] = (-x[t0+k][c0], -x[t0+k][c0+1]) as an f32 pair
+    uint64_t x[16];
+    if (live) {
 #pragma unroll
-        for (int b = 0; b < 16; ++b) {
-          const uint8_t byte = static_cast<uint8_t>(ws[b >> 2] >> ((b & 3) * 8));
-          dst[b] = __fmul_rn(e4m3_to_f32(byte), sc);
+      for (int k = 0; k < 16; ++k) {
+        const int t = tg * 16 + k;
+        if constexpr (kSrc == 0) {
+          const uint32_t b = *reinterpret_cast<const uint16_t*>(sl.st + t * kTile + c0);
+          const float2 f = e4m3x2_to_f32(b);
+          const float nts = -reinterpret_cast<const float*>(sl.st + kTileBytes)[t];  // token scale, negated
+          x[k] = mul2(pk2(f.x, f.y), pk2(nts, nts));
+        } else if constexpr (kSrc == 1) {
+          x[k] = neg_bf16x2(*reinterpret_cast<const uint32_t*>(sl.st + (t * kTile + c0) * 2));
+        } else {
+          const float2 f = *reinterpret_cast<const float2*>(sl.st + (t * kTile + c0) * 4);
+          x[k] = pk2(-f.x, -f.y);
         }
-      } else {
-#pragma unroll
-        for (int b = 0; b < 16; ++b) dst[b] = 0.0f;
       }
     }
-  } else {
-    constexpr bool kF32 = (kSrc == 2);
-    constexpr size_t esz = kF32 ? 4 : 2;
-    const char* sp = static_cast<const char*>(src) + g * T * C * esz;
+    float a0 = 0.0f, a1 = 0.0f;
+    if (live) {
+      if (t0 + 16 > valid) {  // the tile straddles the group's last valid row
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          if (t0 + k >= valid) x[k] = kNegZero2;
+      }
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float2 f = unpk2(x[k]);
+        a0 = fmaxf(a0, fabsf(f.x));
+        a1 = fmaxf(a1, fabsf(f.y));
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) x[k] = kNegZero2;
+    }
+    release(sl, lane);
+    float* rb = sl.red + (sl.it & 1) * 8 * kTile;
+    *reinterpret_cast<float2*>(rb + tg * kTile + c0) = make_float2(a0, a1);
+    if (!exchange(sl, p, lane)) return false;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int idx = tid + i * 256;      // 2048 chunks of 8 elements
-      const int t = idx >> 4, c8 = idx & 15;
-      const int64_t tok = tb * kTile + t;
-      float* dst = xs + t * kRqStride + c8 * 8;
-      float v[8];
-      if (tok < valid) {
-        load8<kF32>(sp + (tok * C + cb * kTile + c8 * 8) * esz, v);
-      } else {
+      const float2 t = *reinterpret_cast<const float2*>(rb + i * kTile + c0);
+      a0 = fmaxf(a0, t.x);
+      a1 = fmaxf(a1, t.y);
+    }
+    const float s0 = tile_scale(a0, a.pow2 != 0), s1 = tile_scale(a1, a.pow2 != 0);
+    const int64_t ch = static_cast<int64_t>(w.d1) * kTile + c0;  // channel index within the group
+    if (tg == 0) {
+      float* sr = a.sT + (g * a.TB + w.d0) * a.ld_c + ch;
+      sr[0] = s0;
+      sr[1] = s1;
+    }
+    const int m0 = make_tile_div_mode(s0), m1 = make_tile_div_mode(s1);
+    const int path = warp_quot_mode(m0 == kQuotDiv || m1 == kQuotDiv ? kQuotDiv
+                                    : (m0 == kQuotMul && m1 == kQuotMul ? kQuotMul : kQuotFma));
+    // per-lane scale pair (channel c0 in the low half, c0+1 in the high half)
+    const float r0 = __frcp_rn(s0), r1 = __frcp_rn(s1);
+    if (path == kQuotMul) {
+      const uint64_t nr2 = pk2(-r0, -r1);
 #pragma unroll
-        for (int b = 0; b < 8; ++b) v[b] = 0.0f;
+      for (int k = 0; k < 16; ++k) x[k] = mul2(x[k], nr2);
+    } else if (path == kQuotFma) {
+      const uint64_t s2 = pk2(s0, s1), nr2 = pk2(-r0, -r1);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) x[k] = quot2_fma(x[k], s2, nr2);
+    } else {
+      const TileDiv d0{s0, r0, m0}, d1{s1, r1, m1};
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float2 f = unpk2(x[k]);
+        x[k] = pk2(tile_quot(-f.x, d0), tile_quot(-f.y, d1));
       }
-#pragma unroll
-      for (int b = 0; b < 8; ++b) dst[b] = v[b];
     }
-  }
-  __syncthreads();
-
-  // ---- per-channel amax over 128 tokens (two threads per channel)
-  {
-    const int c = tid & 127, half = tid >> 7;
-    float a = 0.0f;
-#pragma unroll 8
-    for (int t = half * 64; t < half * 64 + 64; ++t) a = fmaxf(a, fabsf(xs[t * kRqStride + c]));
-    part[half * kTile + c] = a;
-  }
-  __syncthreads();
-  if (tid < kTile) {
-    const float sc = tile_scale(fmaxf(part[tid], part[kTile + tid]), pow2 != 0);
-    part[tid] = sc;
-    sT[g * TB * ld_c + tb * ld_c + cb * kTile + tid] = sc;
-  }
-  __syncthreads();
-
-  // ---- quantize and write transposed: lane -> channel, 16 tokens per store
-  uint8_t* qg = qT + g * C * T;
+    // x[k] holds (channel c0, channel c0+1) of token k; gather each channel's
+    // 16 tokens into one 16-byte row segment
+    uint32_t lo[4], hi[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int idx = tid + i * 256;  // 1024 = 128 channels x 8 token chunks
-    const int c = (idx & 31) + ((idx >> 8) << 5);
-    const int t16 = (idx >> 5) & 7;
-    const TileDiv d = make_tile_div(part[c]);
-    uint32_t w[4];
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const float* col = xs + (t16 * 16 + b * 4) * kRqStride + c;
-      const uint32_t lo = e4m3x2(tile_quot(col[0], d), tile_quot(col[kRqStride], d));
-      const uint32_t hi = e4m3x2(tile_quot(col[2 * kRqStride], d), tile_quot(col[3 * kRqStride], d));
-      w[b] = lo | (hi << 16);
-    }
-    *reinterpret_cast<uint4*>(qg + (cb * kTile + c) * T + tb * kTile + t16 * 16) =
-        make_uint4(w[0], w[1], w[2], w[3]);
+    for (int k4 = 0; k4 < 4; ++k4)
+      e4m3_transpose4(x[4 * k4], x[4 * k4 + 1], x[4 * k4 + 2], x[4 * k4 + 3], lo[k4], hi[k4]);
+    uint8_t* row0 = a.qT + (g * a.C + ch) * a.T + t0;
+    *reinterpret_cast<uint4*>(row0) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    *reinterpret_cast<uint4*>(row0 + a.T) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    return true;
   }
-}
+};
 
-int grid_for(int64_t work_items, int per_block_items, int num_sms, int blocks_per_sm) {
-  int64_t want = (work_items + per_block_items - 1) / per_block_items;
-  int64_t cap = static_cast<int64_t>(num_sms) * blocks_per_sm;
-  if (want > cap) want = cap;
-  if (want < 1) want = 1;
-  return static_cast<int>(want);
-}
-
-// Raise the requantizer's dynamic shared-memory limit once per device.
-template <int kSrc>
-cudaError_t ensure_requant_attr() {
+// ---------------------------------------------------------------- host side
+// Raise the kernel's dynamic shared-memory limit once per device.
+template <class Op>
+cudaError_t ensure_attr() {
   static std::atomic<uint64_t> done{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
-  e = cudaFuncSetAttribute(requant_128x1_kernel<kSrc>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRqSmem);
+  e = cudaFuncSetAttribute(quant_pipe_kernel<Op>, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<Op>::kSmem);
   if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
   return e;
 }
 
-}  // namespace
-
-cudaError_t launch_quant_1x128(const void* x, bool f32, int64_t M, int64_t K, int64_t ldx, uint8_t* q, float* s,
-                               int64_t lds, int pow2, int num_sms, cudaStream_t stream) {
-  constexpr int kUnroll = 4;
-  const int64_t runs = M * ((K / kTile + 2 * kUnroll - 1) / (2 * kUnroll));
-  if (runs >= (1ll << 32) || M >= (1ll << 32)) return cudaErrorInvalidValue;
-  // 256 threads = 8 warps = 8 work units per pass per block
-  const int grid = grid_for(runs, 8, num_sms, 8);
-  if (f32)
-    quant_1x128_kernel<true, kUnroll><<<grid, 256, 0, stream>>>(x, ldx, M, K, q, s, lds, pow2);
-  else
-    quant_1x128_kernel<false, kUnroll><<<grid, 256, 0, stream>>>(x, ldx, M, K, q, s, lds, pow2);
+template <class Op>
+cudaError_t launch_pipe(const CUtensorMap& tm, const typename Op::Args& a, const Pipe& p, int num_sms,
+                        cudaStream_t stream) {
+  static_assert(Layout<Op>::kSmem <= 227 * 1024, "shared memory budget");
+  cudaError_t e = ensure_attr<Op>();
+  if (e != cudaSuccess) return e;
+  const int64_t grid = a.chunks < num_sms ? a.chunks : num_sms;
+  quant_pipe_kernel<Op><<<static_cast<unsigned>(grid), kThreads, Layout<Op>::kSmem, stream>>>(tm, a, p);
   return cudaGetLastError();
 }
 
+CUtensorMapDataType map_type(int esz) {
+  return esz == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                  : (esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
+}
+
+constexpr int64_t kMaxBlocks = (1ll << 31) - 1;  // block coordinates are 32-bit in the walk
+
+}  // namespace
+
+cudaError_t launch_quant_1x128(const void* x, bool f32, int64_t M, int64_t K, int64_t ldx, uint8_t* q, float* s,
+                               int64_t lds, int pow2, const QuantLaunch& l, cudaStream_t stream) {
+  const int esz = f32 ? 4 : 2;
+  const int rows = f32 ? Quant1x128<true>::kRows : Quant1x128<false>::kRows;
+  if (K / kTile > kMaxBlocks) return cudaErrorInvalidValue;
+  CUtensorMap tm;
+  if (!make_map(&tm, map_type(esz), x, K, M, 1, ldx * esz, M * ldx * esz, kTile, rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  const Pipe p{l.status, l.wait_limit_ns, l.debug_skip_fill};
+  const int KB = static_cast<int>(K / kTile);
+  const int64_t chunks = ((M + rows - 1) / rows) * KB;
+  if (f32) {
+    typename Quant1x128<true>::Args a{chunks, M, K, lds, KB, q, s, pow2};
+    return launch_pipe<Quant1x128<true>>(tm, a, p, l.num_sms, stream);
+  }
+  typename Quant1x128<false>::Args a{chunks, M, K, lds, KB, q, s, pow2};
+  return launch_pipe<Quant1x128<false>>(tm, a, p, l.num_sms, stream);
+}
+
 cudaError_t launch_quant_128x128(const void* w, bool f32, int64_t G, int64_t N, int64_t K, uint8_t* q, float* s,
-                                 int pow2, cudaStream_t stream) {
-  const int64_t blocks = G * ((N + kTile - 1) / kTile) * (K / kTile);
-  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-  if (f32)
-    quant_128x128_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(w, N, K, q, s, pow2);
-  else
-    quant_128x128_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(w, N, K, q, s, pow2);
-  return cudaGetLastError();
+                                 int pow2, const QuantLaunch& l, cudaStream_t stream) {
+  const int esz = f32 ? 4 : 2;
+  const int box_rows = f32 ? Quant128x128<true>::kBoxRows : Quant128x128<false>::kBoxRows;
+  const int64_t NB = (N + kTile - 1) / kTile, KB = K / kTile;
+  if (N > kMaxBlocks || KB > kMaxBlocks) return cudaErrorInvalidValue;
+  CUtensorMap tm;
+  if (!make_map(&tm, map_type(esz), w, K, N, G, K * esz, N * K * esz, kTile, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  const Pipe p{l.status, l.wait_limit_ns, l.debug_skip_fill};
+  if (f32) {
+    typename Quant128x128<true>::Args a{G * NB * KB, N, K, static_cast<int>(NB), static_cast<int>(KB), q, s, pow2};
+    return launch_pipe<Quant128x128<true>>(tm, a, p, l.num_sms, stream);
+  }
+  typename Quant128x128<false>::Args a{G * NB * KB, N, K, static_cast<int>(NB), static_cast<int>(KB), q, s, pow2};
+  return launch_pipe<Quant128x128<false>>(tm, a, p, l.num_sms, stream);
 }
 
 cudaError_t launch_requant_128x1(const void* src, int src_kind, const float* s_src, int64_t ld_t, int64_t G,
                                  int64_t T, int64_t C, const int32_t* valid_rows, uint8_t* qT, float* sT,
-                                 int64_t ld_c, int pow2, cudaStream_t stream) {
-  const int64_t blocks = G * (T / kTile) * (C / kTile);
-  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-  const unsigned grid = static_cast<unsigned>(blocks);
-  cudaError_t e = cudaSuccess;
+                                 int64_t ld_c, int pow2, const QuantLaunch& l, cudaStream_t stream) {
+  const int esz = src_kind == 0 ? 1 : (src_kind == 1 ? 2 : 4);
+  const int box_rows = src_kind == 2 ? Requant128x1<2>::kBoxRows : kTile;
+  const int64_t TB = T / kTile, CB = C / kTile;
+  if (TB > kMaxBlocks || CB > kMaxBlocks) return cudaErrorInvalidValue;
+  CUtensorMap tm;
+  if (!make_map(&tm, map_type(esz), src, C, T, G, C * esz, T * C * esz, kTile, box_rows,
+                CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  const Pipe p{l.status, l.wait_limit_ns, l.debug_skip_fill};
+  const int tb = static_cast<int>(TB), cb = static_cast<int>(CB);
   switch (src_kind) {
-    case 0:
-      e = ensure_requant_attr<0>();
-      if (e != cudaSuccess) return e;
-      requant_128x1_kernel<0><<<grid, 256, kRqSmem, stream>>>(src, s_src, ld_t, T, C, valid_rows, qT, sT, ld_c, pow2);
-      break;
-    case 1:
-      e = ensure_requant_attr<1>();
-      if (e != cudaSuccess) return e;
-      requant_128x1_kernel<1><<<grid, 256, kRqSmem, stream>>>(src, s_src, ld_t, T, C, valid_rows, qT, sT, ld_c, pow2);
-      break;
-    default:
-      e = ensure_requant_attr<2>();
-      if (e != cudaSuccess) return e;
-      requant_128x1_kernel<2><<<grid, 256, kRqSmem, stream>>>(src, s_src, ld_t, T, C, valid_rows, qT, sT, ld_c, pow2);
-      break;
+    case 0: {
+      typename Requant128x1<0>::Args a{G * TB * CB, T, C, ld_t, ld_c, tb, cb, s_src, valid_rows, qT, sT, pow2};
+      return launch_pipe<Requant128x1<0>>(tm, a, p, l.num_sms, stream);
+    }
+    case 1: {
+      typename Requant128x1<1>::Args a{G * TB * CB, T, C, ld_t, ld_c, tb, cb, nullptr, valid_rows, qT, sT, pow2};
+      return launch_pipe<Requant128x1<1>>(tm, a, p, l.num_sms, stream);
+    }
+    default: {
+      typename Requant128x1<2>::Args a{G * TB * CB, T, C, ld_t, ld_c, tb, cb, nullptr, valid_rows, qT, sT, pow2};
+      return launch_pipe<Requant128x1<2>>(tm, a, p, l.num_sms, stream);
+    }
   }
-  return cudaGetLastError();
 }
 
 }  // namespace fp8fg

@@ -24,9 +24,9 @@
  *   - Return codes: FP8FG_OK, or a negative FP8FG_ERR_* value;
  *     fp8fg_last_error_string() describes the last error of the calling
  *     thread.
- *   - Bounded device waits: a GEMM whose internal pipeline wait runs past its
- *     limit records FP8FG_ERR_TIMEOUT in a device status word and exits;
- *     fp8fg_check() synchronizes `stream` and reports it.
+ *   - Bounded device waits: a GEMM or quantizer whose internal pipeline wait
+ *     runs past its limit records FP8FG_ERR_TIMEOUT in a device status word
+ *     and exits; fp8fg_check() synchronizes `stream` and reports it.
  *   - Layouts are row-major. "ld(R)" below is fp8fg_scale_ld(R) = R rounded
  *     up to a multiple of 4: the row stride, in floats, of every per-row
  *     scale array, so that each row of scales starts on a 16-byte boundary
@@ -126,7 +126,7 @@ FP8FG_API int fp8_quant_128x128(const void* w, int w_dtype, int64_t G, int64_t N
  *   qT         [G][C][T] E4M3, written
  *   sT         [G][T/128][ld(C)] float, written: sT[tb][c] scales tokens
  *              [tb*128, tb*128+128) of channel c
- * Requires T % 128 == 0, C % 128 == 0, 16-byte aligned src/qT.
+ * Requires T % 128 == 0, C % 128 == 0, 16-byte aligned src, qT and s_src.
  */
 FP8FG_API int fp8_requant_128x1(const void* src, int src_dtype, const float* s_src,
                       int64_t G, int64_t T, int64_t C, const int32_t* valid_rows,
@@ -249,9 +249,10 @@ FP8FG_API const char* fp8fg_version(void);
  * fp8fg_debug_set -- test hooks (no counterpart in the method):
  *   key 1: wait limit of the bounded device waits, in nanoseconds (value 0
  *          restores the default of 2 s);
- *   key 2: GEMM producer skips the copy of its k-th pipeline fill (value
- *          k >= 0; -1 disables), so that the consumers' bounded waits run
- *          out and the call reports FP8FG_ERR_TIMEOUT without faulting.
+ *   key 2: the TMA producer of every GEMM and quantizer CTA skips the copy
+ *          of its k-th pipeline fill (value k >= 0; -1 disables), so that
+ *          the consumers' bounded waits run out and the call reports
+ *          FP8FG_ERR_TIMEOUT without faulting.
  * Returns FP8FG_OK or FP8FG_ERR_INVALID_ARG.
  */
 FP8FG_API int fp8fg_debug_set(int key, int64_t value);

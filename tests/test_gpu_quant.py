@@ -166,3 +166,94 @@ def test_requant_prefill_activation_sampled(lib):
         qo, so = quant.requant_128x1(q, s, None, True)
         assert np.array_equal(qT[:, tb * 128:(tb + 1) * 128].cpu().numpy(), qo)
         assert np.array_equal(sT[tb, :C].cpu().numpy(), so[0])
+
+
+# ---------------------------------------------------------------- many chunks per CTA
+# The quantizers are persistent: one CTA per SM walks its chunks through a
+# ring of 3-12 shared-memory stages. These sizes give every CTA more chunks
+# than stages, so stages are refilled and barrier phases flip several times.
+@pytest.mark.slow
+@pytest.mark.parametrize("pow2", [False, True])
+def test_quant_1x128_ring_wrap(lib, pow2):
+    x = wl.activations(2432, 8192, seed=5, device="cuda")  # BF16: 19 x 64 chunks, 6 stages
+    _check_1x128(lib, x, pow2)
+
+
+@pytest.mark.slow
+def test_quant_1x128_fp32_ring_wrap(lib):
+    x = wl.activations(1216, 8192, seed=8, device="cuda", dtype=torch.float32)  # 19 x 64 chunks of 64 rows
+    _check_1x128(lib, x, False)
+
+
+@pytest.mark.slow
+def test_quant_128x128_ring_wrap(lib):
+    w = wl.weights((2, 1408, 8192), seed=7, device="cuda")  # 2 x 11 x 64 blocks, 6 stages
+    _check_128x128(lib, w)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("pow2", [False, True])
+def test_requant_ring_wrap(lib, pow2):
+    T, C = 4096, 8192  # E4M3 source: 32 x 64 tiles, 12 stages
+    x = wl.activations(T, C, seed=6, device="cpu", dtype=torch.float32).numpy()
+    q, s = quant.quant_1x128(x)
+    s_pad = np.zeros((C // 128, ld4(T)), np.float32)
+    s_pad[:, :T] = s
+    _check_requant(lib, dev(q).view(torch.float8_e4m3fn)[None], dev(s_pad)[None], q[None], s[None], 1, pow2=pow2)
+
+
+@pytest.mark.slow
+def test_requant_bf16_ring_wrap_with_valid_rows(lib):
+    G, T, C = 3, 1024, 4096  # BF16 source: 3 x 8 x 32 tiles, 6 stages; 1.5 groups valid
+    g_ = wl.normal((G, T, C), seed=9, device="cuda", dtype=torch.bfloat16)
+    _check_requant(lib, g_, None, to_np32(g_), None, G, valid=[1024, 500, 0], pow2=True)
+
+
+# ---------------------------------------------------------------- bounded waits
+def _expect_timeout(fg, call):
+    fg.check()
+    try:
+        fg.debug_set(1, 50_000_000)   # 50 ms wait limit
+        fg.debug_set(2, 0)            # every producer skips its first fill
+        call()
+        with pytest.raises(fg.Fp8fgError) as ei:
+            fg.check()
+        assert ei.value.code == fg.ERR_TIMEOUT
+    finally:
+        fg.debug_set(2, -1)
+        fg.debug_set(1, 0)
+
+
+def test_quantizer_timeouts_report_error_and_context_survives(lib):
+    x = wl.activations(256, 1024, seed=11, device="cuda")
+    w = wl.weights((256, 1024), seed=12, device="cuda")
+    _expect_timeout(lib, lambda: lib.fp8_quant_1x128(x))
+    _expect_timeout(lib, lambda: lib.fp8_quant_128x128(w))
+    _expect_timeout(lib, lambda: lib.fp8_requant_128x1(x))
+    # the context is intact and the next calls are exact
+    _check_1x128(lib, x, False)
+    _check_128x128(lib, w)
+    _check_requant(lib, x, None, to_np32(x)[None], None, 1)
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_requant_signed_zeros_and_zero_channels(lib, pow2):
+    # E4M3 source holding +0 (0x00) and -0 (0x80) codes, an all-zero channel
+    # and an all-(-0) token block; BF16 source with -0 entries.
+    T, C = 256, 256
+    rng = np.random.default_rng(77)
+    q = rng.integers(0, 256, size=(T, C), dtype=np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x7E                 # no NaN codes
+    q[:, 5] = 0x00
+    q[:, 6] = 0x80
+    q[128:, 200] = 0x80
+    q[rng.random((T, C)) < 0.05] = 0x80
+    s = np.exp2(rng.integers(-8, 8, size=(C // 128, T))).astype(np.float32) * 0.75
+    s_pad = np.zeros((C // 128, ld4(T)), np.float32)
+    s_pad[:, :T] = s
+    _check_requant(lib, dev(q).view(torch.float8_e4m3fn)[None], dev(s_pad)[None], q[None], s[None], 1, pow2=pow2)
+    xb = wl.normal((T, C), seed=78, device="cuda", dtype=torch.bfloat16)
+    xb[:, 10] = -0.0
+    xb[:64, 11] = 0.0
+    xb[64:, 11] = -0.0
+    _check_requant(lib, xb, None, to_np32(xb)[None], None, 1, pow2=pow2)
