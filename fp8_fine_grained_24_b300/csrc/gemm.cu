@@ -231,12 +231,21 @@ __device__ __forceinline__ bool reduce_splits(const KArgs& a, const Tile& ti, in
 // acc[j] += partial[j] * sbv[j] * sa            (per-row B scales)
 template <int W, bool kBRow>
 __device__ __forceinline__ void promote(float* acc, const uint32_t (&r)[W], float sc, float sa, const float* sbv) {
+  // Pairs of columns on the packed f32x2 pipe: each element still gets one
+  // IEEE round-to-nearest FMA (and, for per-row B scales, one multiply).
 #pragma unroll
-  for (int j = 0; j < W; ++j) {
-    if constexpr (kBRow)
-      acc[j] = fmaf(__uint_as_float(r[j]) * sbv[j], sa, acc[j]);
-    else
-      acc[j] = fmaf(__uint_as_float(r[j]), sc, acc[j]);
+  for (int j = 0; j < W; j += 2) {
+    const uint64_t p = pk2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+    uint64_t a2 = pk2(acc[j], acc[j + 1]);
+    if constexpr (kBRow) {
+      const float2 b = *reinterpret_cast<const float2*>(sbv + j);
+      a2 = fma2(mul2(p, pk2(b.x, b.y)), pk2(sa, sa), a2);
+    } else {
+      a2 = fma2(p, pk2(sc, sc), a2);
+    }
+    const float2 f = unpk2(a2);
+    acc[j] = f.x;
+    acc[j + 1] = f.y;
   }
 }
 

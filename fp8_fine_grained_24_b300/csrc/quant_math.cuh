@@ -8,6 +8,8 @@
 #include <cuda_fp8.h>
 #include <stdint.h>
 
+#include "common.cuh"
+
 namespace fp8fg {
 
 // Scale of a tile from its amax: fl32(amax / 448) (IEEE division, correctly
@@ -139,31 +141,7 @@ __device__ __forceinline__ void quot_n(float (&v)[N], int path, float s, float r
 }
 
 // ---------------------------------------------------------------- packed
-// Pairs of FP32 values in one 64-bit register for the f32x2 arithmetic of
-// sm_100+ (two IEEE round-to-nearest operations per instruction).
-__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-
-__device__ __forceinline__ float2 unpk2(uint64_t v) {
-  float2 f;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(v));
-  return f;
-}
-
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
+// (pk2, unpk2, mul2, fma2: the f32x2 helpers in common.cuh)
 
 // RN(x/s) for a pair given nx = -x, s2 = (s, s) and nr2 = (-r, -r) with
 // r = RN(1/s): the quot_fma sequence on negated operands. q0 = RN(nx*nr) =
