@@ -51,6 +51,16 @@ struct Cfg {
   static constexpr int kThreads = (2 + kEpiWarps) * 32;
   static constexpr int kAccBufs = (BN == 128) ? 4 : 2;      // TMEM partial-sum buffers
   static constexpr int kTmemCols = 512;                      // whole TMEM: one CTA per SM
+  // BN=256 writes BF16 tiles through shared-memory staging and TMA stores:
+  // each epilogue warp's 32 rows x 128 columns as two 128B-swizzled
+  // 64-column boxes (8 KB). The first kBorrowWarps warps stage into the A
+  // and B buffers of the tile's last pipeline stage, whose MMAs have
+  // completed; that stage is released only once their stores have read it.
+  // The other warps use a dedicated area. So the ring keeps all its stages.
+  static constexpr bool kTmaStore = (BN == 256);
+  static constexpr int kEpiWarpBytes = 32 * kColsPerWarp * 2;
+  static constexpr int kBorrowWarps = kTmaStore ? (BM * BK + BN * BK) / kEpiWarpBytes : 0;  // 6
+  static constexpr int kEpiBytes = kTmaStore ? (kEpiWarps - kBorrowWarps) * kEpiWarpBytes : 0;
   static constexpr int kStages = (BN == 128) ? 6 : (BN == 192 ? 5 : 4);
   static constexpr int kABytes = BM * BK;
   static constexpr int kBBytes = BN * BK;
@@ -58,9 +68,10 @@ struct Cfg {
   static constexpr int kSBBytes = BN * 4;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kStages * kABytes;
-  static constexpr int kOffSA = kOffB + kStages * kBBytes;
+  static constexpr int kOffEpi = kOffB + kStages * kBBytes;     // 1024-aligned (see assert)
+  static constexpr int kOffSA = kOffEpi + kEpiBytes;
   static constexpr int kOffSB = kOffSA + kStages * kSABytes;
-  static constexpr int kOffSbw = kOffSB + kStages * kSBBytes;  // per-warp block-scale staging
+  static constexpr int kOffSbw = kOffSB + kStages * kSBBytes;     // per-warp block-scale staging
   static constexpr int kSbwChunk = 128;                           // K blocks staged at a time
   static constexpr int kOffBar = kOffSbw + kEpiWarps * kSbwChunk * 4;
   // full[S], empty[S], tmem_full[B], tmem_empty[B], drain
@@ -72,6 +83,7 @@ struct Cfg {
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
   static_assert((kOffB % 1024) == 0 && (kABytes % 1024) == 0 && (kBBytes % 1024) == 0,
                 "128-byte swizzled tiles need 1024-byte alignment");
+  static_assert(!kTmaStore || (kOffEpi % 1024) == 0, "swizzled store boxes need 1024-byte alignment");
 };
 
 struct KArgs {
@@ -183,6 +195,53 @@ __device__ __forceinline__ void store_row(const KArgs& a, const Tile& ti, int ro
   }
 }
 
+// BF16 tile rows of one epilogue warp (32 rows x NC columns) through its
+// shared-memory staging area and two TMA stores, when every row of the warp
+// may be written (dense: rows past M are clipped by the tensor map; grouped
+// layouts: no padding or masked rows among the 32). Returns false, having
+// done nothing, otherwise; the caller then stores row by row.
+// Staging layout: box b (columns 64b .. 64b+63) is 32 rows of 128 bytes with
+// the 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r % 8)), so a
+// warp's 16-byte writes of one chunk index hit 8 distinct chunks: conflict
+// free.
+template <int NC>
+__device__ __forceinline__ bool store_tile_tma(const KArgs& a, const Tile& ti, int row_in_tile, int col0, int lane,
+                                               uint8_t* region, const CUtensorMap* tmC, const float (&acc)[NC]) {
+  const int row = ti.m0 + row_in_tile;
+  bool ok = true;
+  if (a.mode == kModeContig) ok = row < a.rows && __ldg(a.m_indices + row) >= 0;
+  if (a.mode == kModeMaskedRows) ok = row < __ldg(a.masked + ti.gC);
+  if (!__all_sync(0xffffffffu, ok)) return false;
+  // the previous tile's stores must have read the staging area, and the
+  // tensor core's reads of a borrowed stage come before these writes
+  if (lane == 0) bulk_wait_read_all();
+  fence_async_shared();
+  __syncwarp();
+#pragma unroll
+  for (int b = 0; b < NC / 64; ++b) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int j = b * 64 + c * 8;
+      uint4 v;
+      v.x = pack_bf16x2(acc[j], acc[j + 1]);
+      v.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
+      v.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
+      v.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
+      *reinterpret_cast<uint4*>(region + b * 4096 + lane * 128 + ((c ^ (lane & 7)) << 4)) = v;
+    }
+  }
+  fence_async_shared();
+  __syncwarp();
+  if (lane == 0) {
+    const int y = ti.m0 + (row_in_tile & ~31);
+#pragma unroll
+    for (int b = 0; b < NC / 64; ++b)
+      tma_store_3d(tmC, smem_u32(region + b * 4096), ti.n0 + col0 + b * 64, y, ti.gC);
+    bulk_commit();
+  }
+  return true;
+}
+
 // Split-K: store this split's FP32 partials, count the arrival of this
 // (tile, epilogue warp) and, in the warp that arrives last, replace acc by
 // the sum of all splits' partials in split order (deterministic). Returns
@@ -253,7 +312,7 @@ template <int BN, bool kBRow, bool kF32, bool kSplit>
 __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
-                    const KArgs a) {
+                    const __grid_constant__ CUtensorMap tmC, const KArgs a) {
   using C = Cfg<BN>;
   constexpr int S = C::kStages;
   constexpr int NB = C::kAccBufs;
@@ -380,6 +439,9 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     float acc[NC];
     uint32_t it = 0;
     bool ok = true;
+    // BF16 tiles go out through shared-memory staging and TMA stores
+    constexpr bool kStage = C::kTmaStore && !kF32 && !kSplit;
+    int held = -1;  // pipeline stage kept for staging (kStage, warps < kBorrowWarps)
     for (int t = blockIdx.x; t < a.num_items && ok; t += gridDim.x) {
       const Tile ti = decode_tile<BN, kSplit>(a, t);
       if (ti.skip) continue;
@@ -432,8 +494,11 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
+        // the staging warps keep the tile's last stage for the epilogue
+        const bool hold = kStage && ew < C::kBorrowWarps && kb + 1 == ti.kb0 + ti.kbc;
+        if (hold) held = static_cast<int>(s);
         if (lane == 0) {
-          mbar_arrive(empty_bar(s));
+          if (!hold) mbar_arrive(empty_bar(s));
           mbar_arrive(tempty_bar(buf));
         }
       }
@@ -441,7 +506,32 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       if constexpr (kSplit) {
         if (!reduce_splits<NC, C::kEpiWarps>(a, ti, row_in_tile, ew, lane, acc)) continue;  // not the last split
       }
-      if (!(a.accumulate && ti.kbc == 0)) store_row<NC, kF32>(a, ti, row_in_tile, col0, acc);
+      bool staged = false;
+      if (!(a.accumulate && ti.kbc == 0)) {
+        if constexpr (kStage) {
+          uint8_t* region;
+          if (held >= 0 && ew < 2)
+            region = smem + C::kOffA + held * C::kABytes + ew * C::kEpiWarpBytes;
+          else if (held >= 0)
+            region = smem + C::kOffB + held * C::kBBytes + (ew - 2) * C::kEpiWarpBytes;
+          else
+            region = smem + C::kOffEpi + (ew - C::kBorrowWarps) * C::kEpiWarpBytes;
+          staged = store_tile_tma<NC>(a, ti, row_in_tile, col0, lane, region, &tmC, acc);
+        }
+        if (!staged) store_row<NC, kF32>(a, ti, row_in_tile, col0, acc);
+      }
+      if (held >= 0) {
+        // release the borrowed stage once this warp's stores have read it
+        if (lane == 0) {
+          if (staged) bulk_wait_read_all();
+          mbar_arrive(empty_bar(held));
+        }
+        held = -1;
+      }
+    }
+    // no store may still be reading shared memory when the CTA exits
+    if constexpr (kStage) {
+      if (lane == 0) bulk_wait_all();
     }
   }
 
@@ -499,7 +589,7 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
   using C = Cfg<BN>;
   const int64_t KB = p.K / BK;
   const int64_t groupsA = (p.mode == kModeMaskedRows || p.mode == kModeMaskedK) ? p.groups : 1;
-  CUtensorMap tmA, tmB, tmSA, tmSB;
+  CUtensorMap tmA, tmB, tmSA, tmSB, tmC;
   bool ok = make_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.A, p.K, p.rows, groupsA, p.K, p.rows * p.K, BK, BM,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.B, p.K, p.N, p.groupsB, p.K, p.N * p.K, BK, BN,
@@ -511,6 +601,13 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
                         KB * ld4(p.N) * 4, BN, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
   } else {
     tmSB = tmSA;  // unused
+  }
+  const int64_t groupsC = (p.mode == kModeMaskedRows || p.mode == kModeMaskedK) ? p.groups : 1;
+  if (C::kTmaStore && !p.out_f32) {
+    ok = ok && make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.C, p.N, p.rows, groupsC, p.N * 2,
+                        p.rows * p.N * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    tmC = tmSA;  // unused
   }
   if (!ok) {
     *detail = "cuTensorMapEncodeTiled failed (driver entry point missing or arguments rejected)";
@@ -555,7 +652,7 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
   }
   a.num_items = a.num_tiles * a.splits;
 
-  using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, KArgs);
+  using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, KArgs);
   KernelFn kernel = nullptr;
   cudaError_t e = cudaSuccess;
   const int variant = (p.b_row ? 4 : 0) + (p.out_f32 ? 2 : 0) + (a.splits > 1 ? 1 : 0);
@@ -580,7 +677,7 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
     return e;
   }
   const int grid = a.num_items < num_sms ? a.num_items : num_sms;
-  kernel<<<grid, C::kThreads, C::kSmem, stream>>>(tmA, tmB, tmSA, tmSB, a);
+  kernel<<<grid, C::kThreads, C::kSmem, stream>>>(tmA, tmB, tmSA, tmSB, tmC, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) *detail = "GEMM kernel launch failed";
   return e;
