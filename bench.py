@@ -169,6 +169,10 @@ class PrefillStep:
         self.qb = [torch.empty((n, K), dtype=torch.uint8, device=device) for n in N_PREFILL]
         self.sb = [torch.empty(((n + 127) // 128, K // 128), dtype=torch.float32, device=device) for n in N_PREFILL]
         self.c = [torch.empty((M, n), dtype=torch.bfloat16, device=device) for n in N_PREFILL]
+        # one zero-filled Stream-K workspace, shared by the step's GEMMs (they
+        # run in order on one stream), sized for the largest need
+        ws_bytes = max(fg.gemm_workspace_size(M, n, K) for n in N_PREFILL)
+        self.ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=device) if ws_bytes else None
         self.flops = sum(gemm_flops(M, n, K) for n in N_PREFILL)
         self.launches = 1 + 2 * len(N_PREFILL)
 
@@ -189,7 +193,8 @@ class PrefillStep:
         timed("quant_1x128", lambda: fg.fp8_quant_1x128_out(self.x, self.qa, self.sa))
         for i in range(len(N_PREFILL)):
             timed("quant_128x128", lambda i=i: fg.fp8_quant_128x128_out(self.w[i], self.qb[i], self.sb[i]))
-            timed("gemm", lambda i=i: fg.fp8_gemm_dense_out(self.qa, self.sa, self.qb[i], self.sb[i], self.c[i]))
+            timed("gemm", lambda i=i: fg.fp8_gemm_dense_out(self.qa, self.sa, self.qb[i], self.sb[i], self.c[i],
+                                                            workspace=self.ws))
 
 
 def run_ours(args, rank, world, local_rank):
@@ -333,7 +338,7 @@ def run_e2e(step, fg, torch, device, steps, barrier):
         fg.fp8_quant_1x128_out(dx, step.qa, step.sa)
         for i in range(len(N_PREFILL)):
             fg.fp8_quant_128x128_out(dw[i], step.qb[i], step.sb[i])
-            fg.fp8_gemm_dense_out(step.qa, step.sa, step.qb[i], step.sb[i], step.c[i])
+            fg.fp8_gemm_dense_out(step.qa, step.sa, step.qb[i], step.sb[i], step.c[i], workspace=step.ws)
             hc[i].copy_(step.c[i], non_blocking=True)
 
     one()
@@ -452,7 +457,7 @@ def run_case(args):
             qa, sa = fg.fp8_quant_1x128(wl.activations(M, K, seed, device=dev))
             qb, sb = fg.fp8_quant_128x128(wl.weights((N, K), seed + 1, device=dev))
             c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-            ws = fg.gemm_workspace(M, N, K, device=dev)
+            ws = None if args.no_workspace else fg.gemm_workspace(M, N, K, device=dev)
             return (lambda: fg.fp8_gemm_dense_out(qa, sa, qb, sb, c, workspace=ws),
                     gemm_bytes(M, N, K), gemm_flops(M, N, K))
         if args.case == "quant1x128":
@@ -532,6 +537,8 @@ def main():
                     help="time a single kernel on --shape instead of the full step")
     ap.add_argument("--shape", default="4096,7168,7168")
     ap.add_argument("--graph-reps", type=int, default=10, help="calls per captured graph in --case mode")
+    ap.add_argument("--no-workspace", action="store_true",
+                    help="--case gemm: pass no Stream-K workspace (tiles are never split along K)")
     ap.add_argument("--no-rotate", action="store_true",
                     help="--case mode: reuse one buffer set (L2-warm when it fits in L2)")
     ap.add_argument("--gpus", type=int, default=1)

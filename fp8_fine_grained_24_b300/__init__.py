@@ -201,7 +201,7 @@ def fp8_requant_128x1(src, s_src=None, valid_rows=None, pow2=False, stream=None)
 
 # ---------------------------------------------------------------- GEMMs
 def gemm_workspace_size(M: int, N: int, K: int) -> int:
-    """Split-K workspace bytes for a dense GEMM on the current device (0: none)."""
+    """Stream-K workspace bytes for a dense GEMM on the current device (0: none)."""
     return int(lib.fp8fg_gemm_workspace_size(M, N, K))
 
 

@@ -48,7 +48,19 @@ template <int BN>
 struct Cfg {
   static constexpr int kColsPerWarp = (BN == 256) ? 128 : 64;
   static constexpr int kEpiWarps = 4 * BN / kColsPerWarp;   // 128: 8, 192: 12, 256: 8
-  static constexpr int kThreads = (2 + kEpiWarps) * 32;
+  // BN=256: 12 warps. Warpgroup 0 (producer, MMA issuer, two idle warps)
+  // hands registers to the two promotion warpgroups with setmaxnreg: a
+  // promotion thread holds 128 FP32 accumulators, and at the 168 registers
+  // of an even split the Stream-K variant spilled in its K loop. The launch
+  // must hold kThreads x kRegsLaunch registers, and 128 x kRegsLow +
+  // 256 x kRegsHigh must not exceed that (checked on the host against the
+  // compiled register count before the first launch).
+  static constexpr bool kRegSplit = (BN == 256);
+  static constexpr int kEpiWarp0 = kRegSplit ? 4 : 2;        // first promotion warp
+  static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
+  static constexpr int kRegsLaunch = 168, kRegsLow = 48, kRegsHigh = 224;
+  static_assert(!kRegSplit || (kEpiWarps == 8 && 128 * kRegsLow + 256 * kRegsHigh <= kThreads * kRegsLaunch),
+                "register split exceeds the launch allocation");
   static constexpr int kAccBufs = (BN == 128) ? 4 : 2;      // TMEM partial-sum buffers
   static constexpr int kTmemCols = 512;                      // whole TMEM: one CTA per SM
   // BN=256 writes BF16 tiles through shared-memory staging and TMA stores:
@@ -102,25 +114,31 @@ struct KArgs {
   uint32_t* status;
   uint64_t wait_limit_ns;
   int debug_skip_fill;
-  // split-K (dense only): work item i covers tile i % num_tiles and K-split
-  // i / num_tiles; FP32 partials go to ws_partial[split][row][col] and the
-  // last of the `splits` arrivals per (tile, epilogue warp) reduces them.
-  int splits, num_items;
+  // Stream-K (dense only, the kSplit variant): tiles [0, dp_tiles) run
+  // whole, tile t on CTA t % gridDim.x; the K blocks of tiles sk_tile0 ..
+  // are sk_units "units" in tile-major order and CTA c takes units
+  // [c * sk_per_cta, (c + 1) * sk_per_cta). A tile whose units fall to
+  // several CTAs is summed, in piece order, by the last piece to arrive,
+  // from FP32 partials in ws_partial (one slot per segment, see reduce_sk).
+  int KB;
+  int dp_tiles;
+  int sk_tile0;                      // first split tile (the tiles before it run whole)
+  int sk_units, sk_per_cta, sk_lcm;  // the planner keeps them below 2^31
   float* ws_partial;
   int* ws_count;
 };
 
 struct Tile {
-  int gA, gB, gC, m0, n0, kb0, kbc, tile, split;
+  int gA, gB, gC, m0, n0, kb0, kbc, tile;
+  int sk_start;  // Stream-K segment: its first unit; -1 for a whole tile
   bool skip;
 };
 
-template <int BN, bool kSplit>
-__device__ __forceinline__ Tile decode_tile(const KArgs& a, int item) {
+template <int BN>
+__device__ __forceinline__ Tile decode_tile(const KArgs& a, int t) {
   Tile ti;
-  const int t = kSplit ? item % a.num_tiles : item;
   ti.tile = t;
-  ti.split = kSplit ? item / a.num_tiles : 0;
+  ti.sk_start = -1;
   const int per_group = a.tiles_m * a.tiles_n;
   const int g = t / per_group;
   const int r = t - g * per_group;
@@ -128,14 +146,8 @@ __device__ __forceinline__ Tile decode_tile(const KArgs& a, int item) {
   const int nb = r / a.tiles_m;
   ti.m0 = mb * BM;
   ti.n0 = nb * BN;
-  const int KB = a.K / BK;
-  if constexpr (kSplit) {
-    ti.kb0 = static_cast<int>(static_cast<int64_t>(KB) * ti.split / a.splits);
-    ti.kbc = static_cast<int>(static_cast<int64_t>(KB) * (ti.split + 1) / a.splits) - ti.kb0;
-  } else {
-    ti.kb0 = 0;
-    ti.kbc = KB;
-  }
+  ti.kb0 = 0;
+  ti.kbc = a.KB;
   ti.skip = false;
   ti.gA = ti.gB = ti.gC = 0;
   if (a.mode == kModeContig) {
@@ -153,6 +165,51 @@ __device__ __forceinline__ Tile decode_tile(const KArgs& a, int item) {
     ti.kbc = kbc < ti.kbc ? kbc : ti.kbc;
   }
   return ti;
+}
+
+// This CTA's work in order: whole tiles t = blockIdx.x + i * gridDim.x below
+// dp_tiles (all tiles without Stream-K), then its Stream-K unit range cut at
+// tile boundaries into segments.
+struct Work {
+  int t, u, end;
+};
+
+template <bool kSK>
+__device__ __forceinline__ Work work_begin(const KArgs& a) {
+  Work w;
+  w.t = blockIdx.x;
+  w.u = w.end = 0;
+  if constexpr (kSK) {
+    const int64_t u = static_cast<int64_t>(blockIdx.x) * a.sk_per_cta;
+    const int64_t e = u + a.sk_per_cta;
+    w.u = static_cast<int>(u < a.sk_units ? u : a.sk_units);
+    w.end = static_cast<int>(e < a.sk_units ? e : a.sk_units);
+  }
+  return w;
+}
+
+template <int BN, bool kSK>
+__device__ __forceinline__ bool work_next(const KArgs& a, Work& w, Tile& ti) {
+  const int dp = kSK ? a.dp_tiles : a.num_tiles;
+  if (w.t < dp) {
+    ti = decode_tile<BN>(a, w.t);
+    w.t += gridDim.x;
+    return true;
+  }
+  if constexpr (kSK) {
+    if (w.u < w.end) {
+      const int tt = w.u / a.KB;
+      const int kb0 = w.u - tt * a.KB;
+      const int left = w.end - w.u;
+      ti = decode_tile<BN>(a, a.sk_tile0 + tt);
+      ti.kb0 = kb0;
+      ti.kbc = left < a.KB - kb0 ? left : a.KB - kb0;
+      ti.sk_start = w.u;
+      w.u += ti.kbc;
+      return true;
+    }
+  }
+  return false;
 }
 
 // Convert and store one epilogue thread's share of a tile row.
@@ -242,40 +299,50 @@ __device__ __forceinline__ bool store_tile_tma(const KArgs& a, const Tile& ti, i
   return true;
 }
 
-// Split-K: store this split's FP32 partials, count the arrival of this
-// (tile, epilogue warp) and, in the warp that arrives last, replace acc by
-// the sum of all splits' partials in split order (deterministic). Returns
-// true in the warp that must store the final result. The counter is reset
-// to 0 by that warp, so the workspace stays zeroed between calls.
-// Partials are kept in the threads' own register order: slot
-// [split][tile][warp][j/4][lane] of float4, so every store and load of a
-// warp is one contiguous 512-byte access.
+// Stream-K slots: segments are numbered in unit order; a segment starting
+// at unit s is preceded by the tile boundaries (multiples of KB) and CTA
+// boundaries (multiples of sk_per_cta) in (0, s], counted by inclusion-
+// exclusion over their common multiples (sk_lcm). A slot holds a BM x BN
+// FP32 partial tile in the threads' register order, [warp][j/4][lane]
+// float4, so every store and load of a warp is one contiguous 512-byte
+// access.
+__device__ __forceinline__ int64_t sk_slot(const KArgs& a, int s) {
+  return static_cast<int64_t>(s / a.KB + s / a.sk_per_cta - s / a.sk_lcm);
+}
+
+// Store this segment's partials, count the arrival of this (tile, epilogue
+// warp) and, in the warp that arrives last, replace acc by the sum of all
+// pieces' partials in piece order (deterministic). Returns true in the warp
+// that must store the final result. The counter is reset to 0 by that warp,
+// so the workspace stays zeroed between calls.
 template <int NC, int EW>
-__device__ __forceinline__ bool reduce_splits(const KArgs& a, const Tile& ti, int row_in_tile, int ew, int lane,
-                                              float (&acc)[NC]) {
+__device__ __forceinline__ bool sk_reduce(const KArgs& a, const Tile& ti, int row_in_tile, int ew, int lane,
+                                          float (&acc)[NC]) {
+  constexpr int64_t kSlot = static_cast<int64_t>(EW) * (NC / 4) * 32;  // float4 per slot
   const bool row_ok = ti.m0 + row_in_tile < a.rows;
-  const int64_t per_split = static_cast<int64_t>(a.num_tiles) * EW * (NC / 4) * 32;  // float4 units
-  const int64_t my_off = (static_cast<int64_t>(ti.tile) * EW + ew) * (NC / 4) * 32 + lane;
-  float4* ws4 = reinterpret_cast<float4*>(a.ws_partial);
+  float4* ws4 = reinterpret_cast<float4*>(a.ws_partial) + static_cast<int64_t>(ew) * (NC / 4) * 32 + lane;
   if (row_ok) {
-    float4* mine = ws4 + ti.split * per_split + my_off;
+    float4* mine = ws4 + sk_slot(a, ti.sk_start) * kSlot;
 #pragma unroll
     for (int j = 0; j < NC; j += 4) __stcg(mine + (j / 4) * 32, make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]));
   }
   __threadfence();
   __syncwarp();
-  int* counter = a.ws_count + static_cast<int64_t>(ti.tile) * 16 + ew;
+  const int tt = ti.tile - a.sk_tile0;  // Stream-K tile index
+  const int f = tt * a.KB;              // its first unit
+  const int cf = f / a.sk_per_cta, cl = (f + a.KB - 1) / a.sk_per_cta;
+  int* counter = a.ws_count + tt * 16 + ew;
   int prev = 0;
   if (lane == 0) prev = atomicAdd(counter, 1);
   prev = __shfl_sync(0xffffffffu, prev, 0);
-  if (prev != a.splits - 1) return false;
+  if (prev != cl - cf) return false;
   __threadfence();
   if (lane == 0) *counter = 0;
 #pragma unroll
   for (int j = 0; j < NC; ++j) acc[j] = 0.0f;
   if (row_ok) {
-    for (int sp = 0; sp < a.splits; ++sp) {
-      const float4* src = ws4 + sp * per_split + my_off;
+    for (int c = cf; c <= cl; ++c) {
+      const float4* src = ws4 + sk_slot(a, c == cf ? f : c * a.sk_per_cta) * kSlot;
 #pragma unroll
       for (int j = 0; j < NC; j += 4) {
         const float4 v = __ldcg(src + (j / 4) * 32);
@@ -358,14 +425,17 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
-  if (warp == 0) {
+  if (warp < C::kEpiWarp0) {
+   if constexpr (C::kRegSplit) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsLow));
+   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       constexpr uint32_t tx = C::kABytes + C::kBBytes + C::kSABytes + (kBRow ? C::kSBBytes : 0);
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < a.num_items && ok; t += gridDim.x) {
-        const Tile ti = decode_tile<BN, kSplit>(a, t);
+      Work wk = work_begin<kSplit>(a);
+      Tile ti;
+      while (ok && work_next<BN, kSplit>(a, wk, ti)) {
         if (ti.skip) continue;
         for (int kb = ti.kb0; kb < ti.kb0 + ti.kbc; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1;
@@ -389,14 +459,15 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         mbar_wait(full_bar(i % S), (i / S) & 1, nullptr, 0, a.wait_limit_ns);
       }
     }
-  } else if (warp == 1) {
+   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = f8_idesc(BM, BN);
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < a.num_items && ok; t += gridDim.x) {
-        const Tile ti = decode_tile<BN, kSplit>(a, t);
+      Work wk = work_begin<kSplit>(a);
+      Tile ti;
+      while (ok && work_next<BN, kSplit>(a, wk, ti)) {
         if (ti.skip) continue;
         for (int kb = ti.kb0; kb < ti.kb0 + ti.kbc; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1;
@@ -422,10 +493,12 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       mma_commit(drain_bar);
       if (!mbar_wait(drain_bar, 0, nullptr, 0, a.wait_limit_ns)) atomicCAS(a.status, 0u, kStatusTimeoutDrain);
     }
+   }
   } else {
+    if constexpr (C::kRegSplit) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsHigh));
     // ------------------------------------------------------------ promotion + epilogue
     constexpr int NC = C::kColsPerWarp;
-    const int ew = warp - 2;
+    const int ew = warp - C::kEpiWarp0;
     const int quarter = warp & 3;               // TMEM lanes this warp may access
     const int col0 = (ew >> 2) * NC;            // column group of the tile
     const int row_in_tile = quarter * 32 + lane;
@@ -440,24 +513,29 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     uint32_t it = 0;
     bool ok = true;
     // BF16 tiles go out through shared-memory staging and TMA stores
-    constexpr bool kStage = C::kTmaStore && !kF32 && !kSplit;
+    constexpr bool kStage = C::kTmaStore && !kF32;
     int held = -1;  // pipeline stage kept for staging (kStage, warps < kBorrowWarps)
-    for (int t = blockIdx.x; t < a.num_items && ok; t += gridDim.x) {
-      const Tile ti = decode_tile<BN, kSplit>(a, t);
+    Work wk = work_begin<kSplit>(a);
+    Tile ti;
+    while (ok && work_next<BN, kSplit>(a, wk, ti)) {
       if (ti.skip) continue;
 #pragma unroll
       for (int j = 0; j < NC; ++j) acc[j] = 0.0f;
-      for (int kb = ti.kb0; kb < ti.kb0 + ti.kbc; ++kb, ++it) {
+      // K blocks kb0 .. kb0+kbc-1 by their offset jb in the tile's range:
+      // written this way the loop compiles the same whether kb0 is the
+      // constant 0 (whole tiles) or a Stream-K segment start
+      const int kb0 = ti.kb0, kbc = ti.kbc;
+      for (unsigned jb = 0; jb < static_cast<unsigned>(kbc); ++jb, ++it) {
         const uint32_t s = it % S, ph = (it / S) & 1;
         const uint32_t buf = it % NB, tph = (it / NB) & 1;
-        if (!kBRow && ((kb - ti.kb0) % C::kSbwChunk) == 0) {
+        if (!kBRow && (jb % C::kSbwChunk) == 0) {
           const int nbk = (ti.n0 + col0) / 128;
-          const float* src = a.sB + (static_cast<int64_t>(ti.gB) * a.sb_nblk + nbk) * a.sb_kblk;
+          const float* src = a.sB + (static_cast<int64_t>(ti.gB) * a.sb_nblk + nbk) * a.sb_kblk + kb0;
           __syncwarp();
 #pragma unroll
           for (int i = 0; i < C::kSbwChunk / 32; ++i) {
-            const int k = kb + i * 32 + lane;
-            sbw[i * 32 + lane] = (nbk < a.sb_nblk && k < ti.kb0 + ti.kbc) ? __ldg(src + k) : 0.0f;
+            const unsigned k = jb + i * 32 + lane;
+            sbw[i * 32 + lane] = (nbk < a.sb_nblk && k < static_cast<unsigned>(kbc)) ? __ldg(src + k) : 0.0f;
           }
           __syncwarp();
         }
@@ -469,7 +547,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         }
         const float sa = smem_sa[s * BM + row_in_tile];
         float sc = 0.0f;
-        if constexpr (!kBRow) sc = sa * sbw[(kb - ti.kb0) % C::kSbwChunk];
+        if constexpr (!kBRow) sc = sa * sbw[jb % C::kSbwChunk];
         const float* sbv = smem_sb + s * BN + col0;
         const uint32_t taddr = tmem_base + lane_bits + buf * BN + col0;
         tc_fence_after();
@@ -495,7 +573,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         tc_fence_before();
         __syncwarp();
         // the staging warps keep the tile's last stage for the epilogue
-        const bool hold = kStage && ew < C::kBorrowWarps && kb + 1 == ti.kb0 + ti.kbc;
+        const bool hold = kStage && ew < C::kBorrowWarps && jb + 1 == static_cast<unsigned>(kbc);
         if (hold) held = static_cast<int>(s);
         if (lane == 0) {
           if (!hold) mbar_arrive(empty_bar(s));
@@ -503,11 +581,13 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         }
       }
       if (!ok) break;
+      bool store = !(a.accumulate && ti.kbc == 0);
       if constexpr (kSplit) {
-        if (!reduce_splits<NC, C::kEpiWarps>(a, ti, row_in_tile, ew, lane, acc)) continue;  // not the last split
+        // a Stream-K piece of a split tile: only the last to arrive stores
+        if (ti.kbc != a.KB) store = sk_reduce<NC, C::kEpiWarps>(a, ti, row_in_tile, ew, lane, acc);
       }
       bool staged = false;
-      if (!(a.accumulate && ti.kbc == 0)) {
+      if (store) {
         if constexpr (kStage) {
           uint8_t* region;
           if (held >= 0 && ew < 2)
@@ -555,32 +635,79 @@ cudaError_t ensure_smem_attr() {
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  using C = Cfg<BN>;
+  if constexpr (C::kRegSplit) {
+    // setmaxnreg.inc waits until the block's launch allocation can cover the
+    // raised counts, forever if it never can: refuse to launch a build whose
+    // register count does not cover the split.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, fp8_gemm_kernel<BN, kBRow, kF32, kSplit>);
+    if (e != cudaSuccess) return e;
+    if (static_cast<long>(fa.numRegs) * C::kThreads < 128L * C::kRegsLow + 256L * C::kRegsHigh)
+      return cudaErrorInvalidConfiguration;
+  }
   e = cudaFuncSetAttribute(fp8_gemm_kernel<BN, kBRow, kF32, kSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg<BN>::kSmem);
   if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
   return e;
 }
 
-// K-splitting for dense problems with too few output tiles to occupy the
-// GPU (decode-sized M): as many splits as fit on the SMs, at least four
-// 128-K blocks each, at most 32.
-int choose_splits(int mode, int64_t rows, int64_t N, int64_t K, int64_t groups, int num_sms, int bn) {
-  if (mode != kModeDense || groups != 1) return 1;
-  const int64_t tiles = ((rows + BM - 1) / BM) * ((N + bn - 1) / bn);
-  if (tiles <= 0 || tiles * 2 > num_sms) return 1;
-  int64_t s = num_sms / tiles;
-  s = s < (K / BK) / 4 ? s : (K / BK) / 4;
-  s = s < 32 ? s : 32;
-  return s < 1 ? 1 : static_cast<int>(s);
+// Work plan of a launch. Without Stream-K: one whole tile per work item,
+// min(tiles, SMs) CTAs. Stream-K (dense only) for decode-sized problems
+// (tiles <= SMs/2) when the caller's workspace holds the partials: every
+// tile is split along K over up to all SMs, at least kMinUnits K blocks per
+// CTA. (Splitting only the last, partly idle wave of larger problems was
+// measured slower than leaving it: the split tiles' FP32 partial stores and
+// the summing cost more than the idle SMs did.)
+struct Plan {
+  bool sk = false;
+  int grid = 0;
+  int dp_tiles = 0;
+  int64_t sk_units = 0, sk_per_cta = 0, sk_lcm = 0;
+  size_t partial_bytes = 0, count_bytes = 0;
+};
+
+constexpr int64_t kMinUnits = 4;
+
+int64_t gcd64(int64_t x, int64_t y) {
+  while (y != 0) {
+    const int64_t t = x % y;
+    x = y;
+    y = t;
+  }
+  return x;
 }
 
-// Partials of every (split, tile): BM x bn floats in thread order, then 16
-// arrival counters per tile.
-size_t split_partial_bytes(int bn, int splits, int64_t num_tiles) {
-  return static_cast<size_t>(splits) * num_tiles * BM * bn * sizeof(float);
-}
-size_t split_workspace_bytes(int bn, int splits, int64_t num_tiles) {
-  return split_partial_bytes(bn, splits, num_tiles) + static_cast<size_t>(num_tiles) * 16 * sizeof(int);
+Plan plan_gemm(int mode, int64_t rows, int64_t N, int64_t K, int64_t groups, int num_sms, int bn,
+               size_t ws_avail) {
+  Plan p;
+  const int64_t KB = K / BK;
+  const int64_t tiles = groups * ((rows + BM - 1) / BM) * ((N + bn - 1) / bn);
+  p.grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+  p.dp_tiles = static_cast<int>(tiles);
+  if (mode != kModeDense || groups != 1 || tiles <= 0 || KB <= 0) return p;
+  const int64_t dp = 0;
+  if (tiles * 2 > num_sms) return p;
+  const int64_t cap = tiles * KB / kMinUnits;
+  const int64_t grid = cap < num_sms ? cap : num_sms;
+  if (grid < 2 * tiles) return p;  // too little K to split usefully
+  const int64_t units = (tiles - dp) * KB;
+  if (units >= (1ll << 31)) return p;  // device-side unit counters are 32-bit
+  const int64_t per = (units + grid - 1) / grid;
+  const int64_t lcm = KB / gcd64(KB, per) * per;
+  const int64_t segs = 1 + (units - 1) / KB + (units - 1) / per - (units - 1) / lcm;
+  const size_t partial = static_cast<size_t>(segs) * BM * bn * sizeof(float);
+  const size_t counts = static_cast<size_t>(tiles - dp) * 16 * sizeof(int);
+  if (partial + counts > ws_avail) return p;
+  p.sk = true;
+  p.grid = static_cast<int>((units + per - 1) / per);
+  p.dp_tiles = static_cast<int>(dp);
+  p.sk_units = units;
+  p.sk_per_cta = per;
+  p.sk_lcm = lcm;
+  p.partial_bytes = partial;
+  p.count_bytes = counts;
+  return p;
 }
 
 template <int BN>
@@ -615,6 +742,7 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
   }
   KArgs a;
   a.mode = p.mode;
+  a.KB = static_cast<int>(KB);
   a.rows = static_cast<int>(p.rows);
   a.N = static_cast<int>(p.N);
   a.K = static_cast<int>(p.K);
@@ -639,45 +767,49 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
   a.status = status;
   a.wait_limit_ns = wait_limit_ns;
   a.debug_skip_fill = debug_skip_fill;
-  a.splits = 1;
+  a.dp_tiles = a.num_tiles;
+  a.sk_tile0 = 0;
+  a.sk_units = a.sk_per_cta = a.sk_lcm = 0;
   a.ws_partial = nullptr;
   a.ws_count = nullptr;
   if (a.num_tiles == 0) return cudaSuccess;
-  const int splits = choose_splits(p.mode, p.rows, p.N, p.K, p.groups, num_sms, BN);
-  if (splits > 1 && p.workspace != nullptr &&
-      p.workspace_bytes >= split_workspace_bytes(BN, splits, a.num_tiles)) {
-    a.splits = splits;
-    a.ws_partial = static_cast<float*>(p.workspace);
-    a.ws_count = reinterpret_cast<int*>(static_cast<char*>(p.workspace) + split_partial_bytes(BN, splits, a.num_tiles));
-  }
-  a.num_items = a.num_tiles * a.splits;
+  const Plan plan = plan_gemm(p.mode, p.rows, p.N, p.K, p.groups, num_sms, BN,
+                              p.workspace != nullptr ? p.workspace_bytes : 0);
 
   using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, KArgs);
-  KernelFn kernel = nullptr;
+  KernelFn kernels[2] = {nullptr, nullptr};  // without / with Stream-K
   cudaError_t e = cudaSuccess;
-  const int variant = (p.b_row ? 4 : 0) + (p.out_f32 ? 2 : 0) + (a.splits > 1 ? 1 : 0);
+  const int variant = (p.b_row ? 4 : 0) + (p.out_f32 ? 2 : 0);
   switch (variant) {
-#define FP8FG_VARIANT(V, R, F, S)                          \
-  case V:                                                  \
-    kernel = fp8_gemm_kernel<BN, R, F, S>;                 \
-    e = ensure_smem_attr<BN, R, F, S>();                   \
+#define FP8FG_VARIANT(V, R, F)                                                   \
+  case V:                                                                        \
+    kernels[0] = fp8_gemm_kernel<BN, R, F, false>;                               \
+    kernels[1] = fp8_gemm_kernel<BN, R, F, true>;                                \
+    e = ensure_smem_attr<BN, R, F, false>();                                     \
+    if (e == cudaSuccess && plan.sk) e = ensure_smem_attr<BN, R, F, true>();     \
     break;
-    FP8FG_VARIANT(0, false, false, false)
-    FP8FG_VARIANT(1, false, false, true)
-    FP8FG_VARIANT(2, false, true, false)
-    FP8FG_VARIANT(3, false, true, true)
-    FP8FG_VARIANT(4, true, false, false)
-    FP8FG_VARIANT(5, true, false, true)
-    FP8FG_VARIANT(6, true, true, false)
-    FP8FG_VARIANT(7, true, true, true)
+    FP8FG_VARIANT(0, false, false)
+    FP8FG_VARIANT(2, false, true)
+    FP8FG_VARIANT(4, true, false)
+    FP8FG_VARIANT(6, true, true)
 #undef FP8FG_VARIANT
   }
   if (e != cudaSuccess) {
     *detail = "cudaFuncSetAttribute(max dynamic shared memory) failed";
     return e;
   }
-  const int grid = a.num_items < num_sms ? a.num_items : num_sms;
-  kernel<<<grid, C::kThreads, C::kSmem, stream>>>(tmA, tmB, tmSA, tmSB, tmC, a);
+  if (!plan.sk) {
+    kernels[0]<<<plan.grid, C::kThreads, C::kSmem, stream>>>(tmA, tmB, tmSA, tmSB, tmC, a);
+  } else {
+    a.dp_tiles = plan.dp_tiles;
+    a.sk_tile0 = plan.dp_tiles;
+    a.sk_units = static_cast<int>(plan.sk_units);
+    a.sk_per_cta = static_cast<int>(plan.sk_per_cta);
+    a.sk_lcm = static_cast<int>(plan.sk_lcm);
+    a.ws_partial = static_cast<float*>(p.workspace);
+    a.ws_count = reinterpret_cast<int*>(static_cast<char*>(p.workspace) + plan.partial_bytes);
+    kernels[1]<<<plan.grid, C::kThreads, C::kSmem, stream>>>(tmA, tmB, tmSA, tmSB, tmC, a);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) *detail = "GEMM kernel launch failed";
   return e;
@@ -699,23 +831,15 @@ int pick_bn(const GemmProblem& p) {
 }  // namespace
 
 size_t gemm_workspace_bytes(int mode, int64_t rows, int64_t N, int64_t K, int64_t groups, int num_sms) {
-  const int bn = pick_bn(GemmProblem{});
-  const int splits = choose_splits(mode, rows, N, K, groups, num_sms, bn);
-  if (splits <= 1) return 0;
-  const int64_t tiles = ((rows + BM - 1) / BM) * ((N + bn - 1) / bn);
-  return split_workspace_bytes(bn, splits, tiles);
+  const Plan plan = plan_gemm(mode, rows, N, K, groups, num_sms, pick_bn(GemmProblem{}), SIZE_MAX);
+  return plan.sk ? plan.partial_bytes + plan.count_bytes : 0;
 }
 
 void gemm_workspace_zero_range(int mode, int64_t rows, int64_t N, int64_t K, int64_t groups, int num_sms,
-                               size_t* offset, size_t* bytes) {
-  const int bn = pick_bn(GemmProblem{});
-  const int splits = choose_splits(mode, rows, N, K, groups, num_sms, bn);
-  *offset = 0;
-  *bytes = 0;
-  if (splits <= 1) return;
-  const int64_t tiles = ((rows + BM - 1) / BM) * ((N + bn - 1) / bn);
-  *offset = split_partial_bytes(bn, splits, tiles);
-  *bytes = split_workspace_bytes(bn, splits, tiles) - *offset;
+                               size_t workspace_bytes, size_t* offset, size_t* bytes) {
+  const Plan plan = plan_gemm(mode, rows, N, K, groups, num_sms, pick_bn(GemmProblem{}), workspace_bytes);
+  *offset = plan.sk ? plan.partial_bytes : 0;
+  *bytes = plan.sk ? plan.count_bytes : 0;
 }
 
 cudaError_t launch_gemm(const GemmProblem& p, uint32_t* status, uint64_t wait_limit_ns, int debug_skip_fill,

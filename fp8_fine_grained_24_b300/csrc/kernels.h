@@ -47,20 +47,22 @@ struct GemmProblem {
   int64_t groupsB;       // groups of B (contig: E; masked: E; dense: 1)
   const int32_t* m_indices;
   const int32_t* masked;
-  void* workspace;          // split-K scratch (zeroed before first use), or nullptr
+  void* workspace;          // Stream-K scratch (zeroed before first use), or nullptr
   size_t workspace_bytes;
 };
 
-// Bytes of split-K workspace launch_gemm uses for this problem (0: no split).
+// Bytes of Stream-K workspace launch_gemm uses for this problem when given
+// enough (0: the problem is not split).
 size_t gemm_workspace_bytes(int mode, int64_t rows, int64_t N, int64_t K, int64_t groups, int num_sms);
 
 // Record the calling thread's last error message (fp8fg_last_error_string).
 void set_last_error(const char* msg);
 
-// Byte range of that workspace that must be zero when a launch starts (the
-// split-arrival counters); *bytes = 0 when the problem does not split.
+// Byte range of a workspace of `workspace_bytes` that must be zero when a
+// launch starts (the arrival counters of the plan that workspace allows);
+// *bytes = 0 when that plan does not split.
 void gemm_workspace_zero_range(int mode, int64_t rows, int64_t N, int64_t K, int64_t groups, int num_sms,
-                               size_t* offset, size_t* bytes);
+                               size_t workspace_bytes, size_t* offset, size_t* bytes);
 
 // Enqueue the GEMM. `status` is a device word that receives timeout codes.
 // Returns cudaSuccess or the first CUDA error; *detail gets a static message.

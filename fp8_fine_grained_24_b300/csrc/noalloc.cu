@@ -11,10 +11,10 @@
 //
 // This entry point takes the same inputs and outputs as fp8_gemm_dense and
 // no workspace. Its scratch is a fixed array in device memory that the
-// library reserves when it is loaded: 24 MiB on every GPU the process uses,
+// library reserves when it is loaded: 64 MiB on every GPU the process uses,
 // held until the process exits. That covers every dense shape on GPUs with
-// up to about 190 SMs (the split-K scratch never exceeds one 128 KB partial
-// tile per SM plus counters). Nothing here calls
+// up to about 170 SMs (the Stream-K scratch holds at most three 128 KB
+// partial tiles per SM plus counters). Nothing here calls
 // cudaMalloc, cudaFree or any routine that allocates.
 //
 // Notes for users:
@@ -35,7 +35,7 @@
 
 namespace {
 
-constexpr size_t kStaticScratchBytes = 24u << 20;  // 24 MiB per device
+constexpr size_t kStaticScratchBytes = 64u << 20;  // 64 MiB per device
 
 // The scratch itself. In host code this name is only a host-side stand-in:
 // its device address comes from cudaGetSymbolAddress (below).
@@ -103,13 +103,13 @@ int fp8_gemm_dense_noalloc(const uint8_t* A, const float* sA, const uint8_t* B, 
   const size_t need = fp8fg::gemm_workspace_bytes(fp8fg::kModeDense, M, N, K, 1, d->num_sms);
   if (need > kStaticScratchBytes) {
     fp8fg::set_last_error(
-        "fp8_gemm_dense_noalloc: this shape needs more split-K scratch than the library's static 24 MiB "
+        "fp8_gemm_dense_noalloc: this shape needs more Stream-K scratch than the library's static 64 MiB "
         "array; use fp8_gemm_dense with a workspace");
     return FP8FG_ERR_UNSUPPORTED_SHAPE;
   }
   if (need > 0) {
     size_t off = 0, bytes = 0;
-    fp8fg::gemm_workspace_zero_range(fp8fg::kModeDense, M, N, K, 1, d->num_sms, &off, &bytes);
+    fp8fg::gemm_workspace_zero_range(fp8fg::kModeDense, M, N, K, 1, d->num_sms, kStaticScratchBytes, &off, &bytes);
     if (bytes > 0) {
       cudaError_t e = cudaMemsetAsync(static_cast<unsigned char*>(d->scratch) + off, 0, bytes,
                                       reinterpret_cast<cudaStream_t>(stream));

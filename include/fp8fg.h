@@ -144,13 +144,18 @@ FP8FG_API int fp8_requant_128x1(const void* src, int src_dtype, const float* s_s
  *   C          [M][N] of out_dtype (BF16 or FP32), written
  *   accumulate 1: C += result (FP32 output only: weight-gradient
  *              accumulation); 0: C = result
- *   workspace  device scratch for splitting K when M is too small to occupy
- *              the GPU (decode): fp8fg_gemm_workspace_size(M, N, K) bytes,
- *              16-byte aligned, zero-filled before its first use; every call
- *              leaves it zero-filled again (re-zero it after a call that
- *              reported FP8FG_ERR_TIMEOUT). Calls that share a workspace must
- *              not overlap on the GPU. NULL, or fewer bytes than that size,
- *              runs the same product without splitting K.
+ *   workspace  device scratch for splitting tiles along K over several SMs
+ *              (Stream-K): when M is too small to occupy the GPU (decode),
+ *              and when the last wave of output tiles would leave SMs idle.
+ *              fp8fg_gemm_workspace_size(M, N, K) bytes, 16-byte aligned,
+ *              zero-filled before its first use; every call leaves its
+ *              counters zero-filled again (re-zero the workspace after a call
+ *              that reported FP8FG_ERR_TIMEOUT). Calls that share a workspace
+ *              must not overlap on the GPU. NULL, or fewer bytes than that
+ *              size, runs the same product without splitting K. Split tiles
+ *              are summed in a fixed order: results are deterministic for a
+ *              given shape and SM count, and differ from the unsplit run by
+ *              FP32 rounding only.
  * Requires K % 128 == 0, N % 8 == 0, 16-byte aligned A, B, C.
  */
 FP8FG_API int fp8_gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
@@ -163,24 +168,25 @@ FP8FG_API int fp8_gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B
  * device memory. (No counterpart in the paper: a deployment convenience of
  * this library.) Some callers only receive device pointers from a host
  * application that owns all device memory and offers no allocator, or run
- * where a device allocation is forbidden; they cannot provide the split-K
+ * where a device allocation is forbidden; they cannot provide the Stream-K
  * workspace. This entry point computes the same product with the same
- * arguments minus the workspace, using instead a 24 MiB array that the
+ * arguments minus the workspace, using instead a 64 MiB array that the
  * library reserves in device memory when it is loaded (on every GPU the
  * process uses, until exit). It allocates nothing.
  *   - The first call on a device looks up that array's device address;
  *     that first call should come before any stream capture.
  *   - All calls share the array: calls whose GPU work overlaps race on it.
  *   - Each call clears the part of the array that must start at zero.
- *   - A shape needing more scratch than 24 MiB is rejected with
- *     FP8FG_ERR_UNSUPPORTED_SHAPE (none exists on GPUs with up to ~190 SMs).
+ *   - A shape needing more scratch than 64 MiB is rejected with
+ *     FP8FG_ERR_UNSUPPORTED_SHAPE (none exists on GPUs with up to ~170 SMs).
  */
 FP8FG_API int fp8_gemm_dense_noalloc(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
                                      int b_scale_kind, void* C, int out_dtype, int accumulate,
                                      int64_t M, int64_t N, int64_t K, fp8fg_stream_t stream);
 
 /* Bytes of workspace fp8_gemm_dense uses for this shape on the current
- * device (0 if it does not split K). Needs a CUDA device; 0 on error. */
+ * device (0 if it does not split tiles along K). Needs a CUDA device; 0 on
+ * error. */
 FP8FG_API size_t fp8fg_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /*

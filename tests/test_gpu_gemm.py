@@ -350,3 +350,45 @@ def test_decode_full_sampled(lib, M, N, K):
         cols = slice(nb * 128, nb * 128 + 128)
         qb, sb = quant.quant_128x128(to_np32(w[cols]))
         compare_gemm(c[:, cols], gemm.gemm_dense(qa, sa, qb, sb), True)
+
+
+# ---------------------------------------------------------------- Stream-K segments
+# Decode-sized problems split every tile along K over the SMs: CTA c takes
+# K blocks [c*U, (c+1)*U) of the tile-major sequence, so when U does not
+# divide the tile's K blocks a CTA's range straddles two tiles and a tile's
+# pieces come from several CTAs; the last piece to arrive sums them in
+# order. On 148 SMs, M=64, N=1792, K=6912 gives 7 tiles of 54 K blocks,
+# U = 5.
+def _sk_case(fg, M, N, K, seed, out_dtype=torch.bfloat16, accumulate=False, rows=None):
+    x = wl.activations(M, K, seed, device="cpu")
+    w = wl.weights((N, K), seed + 1, device="cpu")
+    qa, sa, qa_d, sa_d = _quant_a(x)
+    qb, sb, qb_d, sb_d = _quant_b(w)
+    ws = fg.gemm_workspace(M, N, K)
+    if ws is None:
+        pytest.skip("this GPU's SM count fills the last wave: no Stream-K split")
+    sel = np.arange(M) if rows is None else np.asarray(rows)
+    cref = gemm.gemm_dense(qa, sa, qb, sb, rows=sel)
+    base = torch.randn((M, N), dtype=torch.float32, device="cuda") if accumulate else None
+    outs = []
+    for _ in range(2):  # the arrival counters must come back to zero
+        c = base.clone() if accumulate else torch.empty((M, N), dtype=out_dtype, device="cuda")
+        fg.fp8_gemm_dense_out(qa_d, sa_d, qb_d, sb_d, c, accumulate=accumulate, workspace=ws)
+        torch.cuda.synchronize()
+        ref = cref + base.double().cpu().numpy()[sel] if accumulate else cref
+        compare_gemm(c[torch.as_tensor(sel, device="cuda")], ref, out_dtype == torch.bfloat16)
+        outs.append(c)
+    assert torch.equal(outs[0], outs[1]), "Stream-K result is not deterministic"
+    # the unsplit product agrees within the same tolerance
+    c = base.clone() if accumulate else torch.empty((M, N), dtype=out_dtype, device="cuda")
+    fg.fp8_gemm_dense_out(qa_d, sa_d, qb_d, sb_d, c, accumulate=accumulate, workspace=None)
+    torch.cuda.synchronize()
+    compare_gemm(c[torch.as_tensor(sel, device="cuda")], ref, out_dtype == torch.bfloat16)
+
+
+def test_stream_k_segments_straddle_tiles(lib):
+    _sk_case(lib, 64, 1792, 6912, seed=91)
+
+
+def test_stream_k_straddle_fp32_accumulate(lib):
+    _sk_case(lib, 64, 1792, 6912, seed=93, out_dtype=torch.float32, accumulate=True)
