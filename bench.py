@@ -439,6 +439,9 @@ def run_case(args):
     """Time one kernel on one shape (sweeps and ncu captures): prints one JSON line.
 
     gemm M,N,K        dense GEMM, bf16 out (operands quantized once, untimed)
+    contig E,T,N,K    grouped-contiguous MoE GEMM: T tokens routed by Zipf(1.1) counts
+    masked E,M,N,K    grouped-masked MoE GEMM: uniform counts up to M tokens per expert
+    wgrad E,T,N,C     masked-K weight gradient dW_e = G_e^T X_e (128x1 pow2 operands, FP32 out)
     quant1x128 M,K    activation quantization of bf16 [M, K]
     quant128x128 N,K  weight quantization of bf16 [N, K]
     requant T,C       128x1 requantization of an E4M3 [T, C] with 1x128 scales (pow2)
@@ -460,6 +463,48 @@ def run_case(args):
             ws = None if args.no_workspace else fg.gemm_workspace(M, N, K, device=dev)
             return (lambda: fg.fp8_gemm_dense_out(qa, sa, qb, sb, c, workspace=ws),
                     gemm_bytes(M, N, K), gemm_flops(M, N, K))
+        if args.case == "contig":
+            E, T, N, K = dims
+            counts = wl.zipf_counts(T, E, 1.1, seed)
+            lay = wl.contig_layout(counts)
+            Mt = len(lay.m_indices)
+            qa, sa = fg.fp8_quant_1x128(wl.activations(Mt, K, seed, device=dev))
+            qb, sb = fg.fp8_quant_128x128(wl.weights((E, N, K), seed + 1, device=dev))
+            mi = torch.as_tensor(lay.m_indices, device=dev)
+            c = torch.empty((Mt, N), dtype=torch.bfloat16, device=dev)
+            nb = Mt * K + E * N * K + Mt * (K // 128) * 4 + E * (N // 128) * (K // 128) * 4 + T * N * 2
+            return (lambda: fg.fp8_gemm_grouped_contig_out(qa, sa, qb, sb, mi, c), nb, 2.0 * T * N * K)
+        if args.case == "masked":
+            E, Mmax, N, K = dims
+            counts = wl.masked_counts(E, Mmax, seed)
+            qa, sa = fg.fp8_quant_1x128(wl.activations(E * Mmax, K, seed, device=dev))
+            qa, sa = qa.view(E, Mmax, K), sa.view(K // 128, -1)
+            sa3 = torch.empty((E, K // 128, fg.scale_ld(Mmax)), dtype=torch.float32, device=dev)
+            for e in range(E):
+                sa3[e, :, :Mmax] = sa[:, e * Mmax:(e + 1) * Mmax]
+            qb, sb = fg.fp8_quant_128x128(wl.weights((E, N, K), seed + 1, device=dev))
+            mm = torch.as_tensor(counts, device=dev)
+            c = torch.empty((E, Mmax, N), dtype=torch.bfloat16, device=dev)
+            T = int(counts.sum())
+            nb = T * K + E * N * K + T * N * 2
+            return (lambda: fg.fp8_gemm_grouped_masked_out(qa, sa3, qb, sb, mm, c, expected_m=Mmax), nb,
+                    2.0 * T * N * K)
+        if args.case == "wgrad":
+            # per expert dW_e[N, C] = G_e^T X_e over its valid tokens: operands
+            # requantized to 128x1 tiles with power-of-2 scales, FP32 out
+            E, Tmax, N, C = dims
+            counts = wl.masked_counts(E, Tmax, seed)
+            vr = torch.as_tensor(counts, device=dev)
+            g = wl.normal((E, Tmax, N), seed, device=dev, dtype=torch.bfloat16)
+            x = wl.activations(E * Tmax, C, seed + 1, device=dev).view(E, Tmax, C)
+            qgT, sgT = fg.fp8_requant_128x1(g, None, vr, pow2=True)
+            qxT, sxT = fg.fp8_requant_128x1(x.contiguous(), None, vr, pow2=True)
+            out = torch.zeros((E, N, C), dtype=torch.float32, device=dev)
+            T = int(counts.sum())
+            nb = T * (N + C) + E * N * C * 4
+            return (lambda: fg.fp8_gemm_grouped_masked_out(qgT, sgT, qxT, sxT, vr, out, b_scale_kind=fg.SCALE_ROW,
+                                                           mask_dim=fg.MASK_K, expected_m=Tmax),
+                    nb, 2.0 * T * N * C)
         if args.case == "quant1x128":
             M, K = dims
             x = wl.activations(M, K, seed, device=dev)
@@ -533,7 +578,8 @@ def run_case(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", choices=["gemm", "quant1x128", "quant128x128", "requant"], default=None,
+    ap.add_argument("--case", choices=["gemm", "contig", "masked", "wgrad", "quant1x128", "quant128x128", "requant"],
+                    default=None,
                     help="time a single kernel on --shape instead of the full step")
     ap.add_argument("--shape", default="4096,7168,7168")
     ap.add_argument("--graph-reps", type=int, default=10, help="calls per captured graph in --case mode")

@@ -252,16 +252,17 @@ __device__ __forceinline__ void store_row(const KArgs& a, const Tile& ti, int ro
   }
 }
 
-// BF16 tile rows of one epilogue warp (32 rows x NC columns) through its
-// shared-memory staging area and two TMA stores, when every row of the warp
-// may be written (dense: rows past M are clipped by the tensor map; grouped
+// Tile rows of one epilogue warp (32 rows x NC columns) through its 8 KB
+// shared-memory staging area and TMA stores, when every row of the warp may
+// be written (dense: rows past M are clipped by the tensor map; grouped
 // layouts: no padding or masked rows among the 32). Returns false, having
 // done nothing, otherwise; the caller then stores row by row.
-// Staging layout: box b (columns 64b .. 64b+63) is 32 rows of 128 bytes with
-// the 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r % 8)), so a
-// warp's 16-byte writes of one chunk index hit 8 distinct chunks: conflict
-// free.
-template <int NC>
+// Staging: two boxes of 32 rows x 128 bytes (BF16: 64 columns each; FP32:
+// 32 columns each, so FP32 goes out in two rounds of 64 columns) with the
+// 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r % 8)): a warp's
+// 16-byte writes of one chunk index hit 8 distinct chunks, conflict free.
+// FP32 with accumulate adds into C with the TMA reduce-add.
+template <int NC, bool kF32>
 __device__ __forceinline__ bool store_tile_tma(const KArgs& a, const Tile& ti, int row_in_tile, int col0, int lane,
                                                uint8_t* region, const CUtensorMap* tmC, const float (&acc)[NC]) {
   const int row = ti.m0 + row_in_tile;
@@ -269,32 +270,48 @@ __device__ __forceinline__ bool store_tile_tma(const KArgs& a, const Tile& ti, i
   if (a.mode == kModeContig) ok = row < a.rows && __ldg(a.m_indices + row) >= 0;
   if (a.mode == kModeMaskedRows) ok = row < __ldg(a.masked + ti.gC);
   if (!__all_sync(0xffffffffu, ok)) return false;
-  // the previous tile's stores must have read the staging area, and the
-  // tensor core's reads of a borrowed stage come before these writes
-  if (lane == 0) bulk_wait_read_all();
-  fence_async_shared();
-  __syncwarp();
+  constexpr int kColsPerRound = 64;          // two 128-byte boxes
+  constexpr int kBoxCols = kF32 ? 32 : 64;
+  const int y = ti.m0 + (row_in_tile & ~31);
 #pragma unroll
-  for (int b = 0; b < NC / 64; ++b) {
+  for (int rd = 0; rd < NC / kColsPerRound; rd += (kF32 ? 1 : 2)) {
+    // the previous stores must have read the staging area, and the tensor
+    // core's reads of a borrowed stage come before these writes
+    if (lane == 0) bulk_wait_read_all();
+    fence_async_shared();
+    __syncwarp();
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const int j = b * 64 + c * 8;
-      uint4 v;
-      v.x = pack_bf16x2(acc[j], acc[j + 1]);
-      v.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
-      v.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
-      v.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
-      *reinterpret_cast<uint4*>(region + b * 4096 + lane * 128 + ((c ^ (lane & 7)) << 4)) = v;
+    for (int b = 0; b < 2; ++b) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint4 v;
+        if constexpr (kF32) {
+          const int j = rd * kColsPerRound + b * kBoxCols + c * 4;
+          v = make_uint4(__float_as_uint(acc[j]), __float_as_uint(acc[j + 1]), __float_as_uint(acc[j + 2]),
+                         __float_as_uint(acc[j + 3]));
+        } else {
+          const int j = b * kBoxCols + c * 8;
+          v.x = pack_bf16x2(acc[j], acc[j + 1]);
+          v.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
+          v.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
+          v.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
+        }
+        *reinterpret_cast<uint4*>(region + b * 4096 + lane * 128 + ((c ^ (lane & 7)) << 4)) = v;
+      }
     }
-  }
-  fence_async_shared();
-  __syncwarp();
-  if (lane == 0) {
-    const int y = ti.m0 + (row_in_tile & ~31);
+    fence_async_shared();
+    __syncwarp();
+    if (lane == 0) {
 #pragma unroll
-    for (int b = 0; b < NC / 64; ++b)
-      tma_store_3d(tmC, smem_u32(region + b * 4096), ti.n0 + col0 + b * 64, y, ti.gC);
-    bulk_commit();
+      for (int b = 0; b < 2; ++b) {
+        const int x = ti.n0 + col0 + (kF32 ? rd * kColsPerRound : 0) + b * kBoxCols;
+        if (kF32 && a.accumulate)
+          tma_reduce_add_3d(tmC, smem_u32(region + b * 4096), x, y, ti.gC);
+        else
+          tma_store_3d(tmC, smem_u32(region + b * 4096), x, y, ti.gC);
+      }
+      bulk_commit();
+    }
   }
   return true;
 }
@@ -513,7 +530,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     uint32_t it = 0;
     bool ok = true;
     // BF16 tiles go out through shared-memory staging and TMA stores
-    constexpr bool kStage = C::kTmaStore && !kF32;
+    constexpr bool kStage = C::kTmaStore;
     int held = -1;  // pipeline stage kept for staging (kStage, warps < kBorrowWarps)
     Work wk = work_begin<kSplit>(a);
     Tile ti;
@@ -596,7 +613,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
             region = smem + C::kOffB + held * C::kBBytes + (ew - 2) * C::kEpiWarpBytes;
           else
             region = smem + C::kOffEpi + (ew - C::kBorrowWarps) * C::kEpiWarpBytes;
-          staged = store_tile_tma<NC>(a, ti, row_in_tile, col0, lane, region, &tmC, acc);
+          staged = store_tile_tma<NC, kF32>(a, ti, row_in_tile, col0, lane, region, &tmC, acc);
         }
         if (!staged) store_row<NC, kF32>(a, ti, row_in_tile, col0, acc);
       }
@@ -730,9 +747,11 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
     tmSB = tmSA;  // unused
   }
   const int64_t groupsC = (p.mode == kModeMaskedRows || p.mode == kModeMaskedK) ? p.groups : 1;
-  if (C::kTmaStore && !p.out_f32) {
-    ok = ok && make_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.C, p.N, p.rows, groupsC, p.N * 2,
-                        p.rows * p.N * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (C::kTmaStore) {
+    const int64_t esz = p.out_f32 ? 4 : 2;
+    ok = ok && make_map(&tmC, p.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.C,
+                        p.N, p.rows, groupsC, p.N * esz, p.rows * p.N * esz, 128 / esz, 32,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
   } else {
     tmC = tmSA;  // unused
   }
