@@ -40,6 +40,7 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 128;
+constexpr int kContigBand = 16;  // M blocks per raster band of the grouped-contiguous layout
 
 // Tile configurations. The epilogue warps split the tile's columns in
 // groups of kColsPerWarp; four warps (one per TMEM lane quarter) share a
@@ -142,8 +143,22 @@ __device__ __forceinline__ Tile decode_tile(const KArgs& a, int t) {
   const int per_group = a.tiles_m * a.tiles_n;
   const int g = t / per_group;
   const int r = t - g * per_group;
-  const int mb = r % a.tiles_m;
-  const int nb = r / a.tiles_m;
+  int mb, nb;
+  if (a.mode == kModeContig) {
+    // grouped raster: bands of kContigBand M blocks, M fastest inside a band.
+    // A band's rows (a few experts) stay in L2 while its N blocks pass, and
+    // each expert's B tiles are read about once per band. (M fastest over
+    // all rows, as for dense problems, re-read the whole of A every wave.)
+    const int band = r / (kContigBand * a.tiles_n);
+    const int m_first = band * kContigBand;
+    const int rows = a.tiles_m - m_first < kContigBand ? a.tiles_m - m_first : kContigBand;
+    const int rr = r - band * kContigBand * a.tiles_n;
+    mb = m_first + rr % rows;
+    nb = rr / rows;
+  } else {
+    mb = r % a.tiles_m;
+    nb = r / a.tiles_m;
+  }
   ti.m0 = mb * BM;
   ti.n0 = nb * BN;
   ti.kb0 = 0;
