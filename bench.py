@@ -46,9 +46,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # reported traffic is null. Writes sit below M*N*2 because output lines still
 # in L2 when the kernel ends are written back after it.
 NCU_TRAFFIC = {
-    "kernel_sha": "51f5fbc60351eb75",
-    "per_launch": {2112: 45507072 + 1057280, 24576: 211726592 + 177846784,
-                   7168: 82550784 + 34114560, 4096: 60004864 + 8921856},
+    "kernel_sha": "b56ab55cb7560ed1",
+    "per_launch": {2112: 45535744 + 1134336, 24576: 210937088 + 179328512,
+                   7168: 82958848 + 36564224, 4096: 60056320 + 10929920},
 }
 
 
