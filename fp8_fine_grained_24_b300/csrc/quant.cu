@@ -37,9 +37,8 @@ namespace fp8fg {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kConsumerWarps = 16;
-constexpr int kThreads = 32 * (1 + kConsumerWarps);
-constexpr int kRingBytes = 192 * 1024;
+constexpr int kConsumerWarps = 16;     // the 1x128 and 128x128 quantizers
+constexpr int kRingBytes = 192 * 1024;  // per SM
 
 enum : uint32_t { kStatusTimeoutQuantProducer = 5, kStatusTimeoutQuantConsumer = 6, kStatusTimeoutQuantDrain = 7 };
 
@@ -116,44 +115,53 @@ __device__ __forceinline__ uint2 codes8(const uint64_t (&v)[4]) {
 
 // ---------------------------------------------------------------- pipeline
 // Shared memory: kStages stages of kStageBytes, then full[S], empty[S] and
-// one exchange barrier (8 bytes each), then the exchange buffer.
+// Op::kExchBars exchange barriers (8 bytes each), then the exchange buffer.
 template <class Op>
 struct Layout {
   static constexpr int kBarOff = Op::kStages * Op::kStageBytes;
-  static constexpr int kRedOff = (kBarOff + (2 * Op::kStages + 1) * 8 + 15) / 16 * 16;
+  static constexpr int kRedOff = (kBarOff + (2 * Op::kStages + Op::kExchBars) * 8 + 15) / 16 * 16;
   static constexpr int kSmem = kRedOff + Op::kRedBytes;
 };
 
+// The pipeline's dynamic shared memory. Stages and the exchange buffer are
+// addressed as offsets into this array (not through pointers kept in
+// structs), so that every consumer access compiles to a shared-memory load
+// rather than a generic one.
+extern __shared__ __align__(1024) uint8_t quant_smem[];
+
 // Per-chunk context handed to a consumer.
 struct Slot {
-  const uint8_t* st;  // the stage's shared memory
+  uint32_t st_off;  // the stage: byte offset in quant_smem
   uint32_t full, empty, ph;
   uint32_t red_bar;
-  float* red;
-  uint32_t it;  // this CTA's chunk counter (exchange-buffer parity)
+  uint32_t red_off;  // the exchange buffer: byte offset in quant_smem
+  uint32_t it;       // this CTA's chunk counter (exchange-buffer parity)
 };
 
-// Warp 0 lane 0 fills stages; warps 1..16 consume them in the same chunk
-// order (chunk c = blockIdx.x + i * gridDim.x).
+__device__ __forceinline__ const uint8_t* stage_of(const Slot& sl) { return quant_smem + sl.st_off; }
+__device__ __forceinline__ float* red_of(const Slot& sl) { return reinterpret_cast<float*>(quant_smem + sl.red_off); }
+
+// Warp 0 lane 0 fills stages; warps 1..Op::kWarps consume them in the same
+// chunk order (chunk c = blockIdx.x + i * gridDim.x). Op::kCtasPerSm CTAs
+// share an SM.
 template <class Op>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(32 * (1 + Op::kWarps), Op::kCtasPerSm)
     quant_pipe_kernel(const __grid_constant__ CUtensorMap tm, const typename Op::Args a, const Pipe p) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* const smem = quant_smem;
   constexpr int S = Op::kStages;
   using L = Layout<Op>;
   const uint32_t base = smem_u32(smem);
   const uint32_t bar0 = base + L::kBarOff;
   const uint32_t red_bar = bar0 + 2 * S * 8;
-  float* red = reinterpret_cast<float*>(smem + L::kRedOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t chunks = a.chunks;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(bar0 + s * 8, 1);
-      mbar_init(bar0 + (S + s) * 8, kConsumerWarps);
+      mbar_init(bar0 + (S + s) * 8, Op::kWarps);
     }
-    mbar_init(red_bar, kConsumerWarps);
+    for (int i = 0; i < Op::kExchBars; ++i) mbar_init(red_bar + i * 8, Op::kWarps);
     fence_barrier_init();
   }
   __syncthreads();
@@ -187,14 +195,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   const int cw = warp - 1;
+  typename Op::State state{};
+  bool ok = true;
   for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x, ++it, w.advance()) {
-    const Slot sl{smem + s * Op::kStageBytes, bar0 + s * 8, bar0 + (S + s) * 8, ph, red_bar, red, it};
-    if (!Op::consume(a, p, w, sl, cw, lane)) break;
+    const Slot sl{s * Op::kStageBytes, bar0 + s * 8, bar0 + (S + s) * 8, ph, red_bar, L::kRedOff, it};
+    if (!Op::consume(a, p, w, sl, cw, lane, state)) {
+      ok = false;
+      break;
+    }
     if (++s == S) {
       s = 0;
       ph ^= 1;
     }
   }
+  if (ok) Op::finish(a, p, cw, lane, state);
 }
 
 __device__ __forceinline__ bool wait_full(const Slot& sl, const Pipe& p) {
@@ -236,9 +250,12 @@ struct Quant1x128 {
   static constexpr int kEsz = kF32 ? 4 : 2;
   static constexpr int kRows = kF32 ? 64 : 128;
   static constexpr int kStageBytes = kRows * kTile * kEsz;
+  static constexpr int kWarps = kConsumerWarps, kCtasPerSm = 1;
   static constexpr int kStages = kRingBytes / kStageBytes;
   static constexpr int kRedBytes = 0;
+  static constexpr int kExchBars = 0;
   static constexpr int kIters = kRows / kConsumerWarps / 2;  // 4 (BF16) or 2 (FP32)
+  struct State {};
   static constexpr int kWarpRows = 2 * kIters;
 
   struct Args {
@@ -260,14 +277,16 @@ struct Quant1x128 {
     tma_load_3d(dst, &tm, full, w.d0 * kTile, static_cast<int32_t>(w.d2 * kRows), 0);
   }
 
+  static __device__ __forceinline__ void finish(const Args&, const Pipe&, int, int, State&) {}
+
   static __device__ __forceinline__ bool consume(const Args& a, const Pipe& p, const Walk& w, const Slot& sl,
-                                                 int cw, int lane) {
+                                                 int cw, int lane, State&) {
     const int half = lane >> 4, j = lane & 15;
     if (!wait_full(sl, p)) return false;
     uint64_t v[kIters][4];
 #pragma unroll
     for (int i = 0; i < kIters; ++i)
-      load_neg8<kF32>(sl.st + ((cw * kWarpRows + 2 * i + half) * kTile + j * 8) * kEsz, v[i]);
+      load_neg8<kF32>(stage_of(sl) + ((cw * kWarpRows + 2 * i + half) * kTile + j * 8) * kEsz, v[i]);
     // row maxima: after the xor-shuffles every lane of half h holds am[i] of row 2i+h
     float am[kIters];
 #pragma unroll
@@ -318,9 +337,12 @@ struct Quant128x128 {
   static constexpr int kEsz = kF32 ? 4 : 2;
   static constexpr int kStageBytes = kTile * kTile * kEsz;
   static constexpr int kBoxRows = kF32 ? 64 : 128;
+  static constexpr int kWarps = kConsumerWarps, kCtasPerSm = 1;
   static constexpr int kStages = kRingBytes / kStageBytes;
   static constexpr int kRedBytes = 2 * kConsumerWarps * 4;
+  static constexpr int kExchBars = 1;
   static constexpr int kIters = kTile / kConsumerWarps / 2;
+  struct State {};
 
   struct Args {
     int64_t chunks, N, K;
@@ -344,21 +366,23 @@ struct Quant128x128 {
                   static_cast<int32_t>(w.d2));
   }
 
+  static __device__ __forceinline__ void finish(const Args&, const Pipe&, int, int, State&) {}
+
   static __device__ __forceinline__ bool consume(const Args& a, const Pipe& p, const Walk& w, const Slot& sl,
-                                                 int cw, int lane) {
+                                                 int cw, int lane, State&) {
     const int half = lane >> 4, j = lane & 15;
     if (!wait_full(sl, p)) return false;
     uint64_t v[kIters][4];
 #pragma unroll
     for (int i = 0; i < kIters; ++i)
-      load_neg8<kF32>(sl.st + ((cw * (2 * kIters) + 2 * i + half) * kTile + j * 8) * kEsz, v[i]);
+      load_neg8<kF32>(stage_of(sl) + ((cw * (2 * kIters) + 2 * i + half) * kTile + j * 8) * kEsz, v[i]);
     float am = 0.0f;
 #pragma unroll
     for (int i = 0; i < kIters; ++i) am = fmaxf(am, amax4pk(v[i]));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
     release(sl, lane);
-    float* rb = sl.red + (sl.it & 1) * kConsumerWarps;
+    float* rb = red_of(sl) + (sl.it & 1) * kConsumerWarps;
     if (lane == 0) rb[cw] = am;
     if (!exchange(sl, p, lane)) return false;
     const float4* r4 = reinterpret_cast<const float4*>(rb);
@@ -385,31 +409,45 @@ struct Quant128x128 {
 };
 
 // ------------------------------------------------------------ 128x1
-// Chunk: one 128-token x 128-channel source tile (E4M3 16 KB, BF16 32 KB,
-// FP32 two 64-token boxes), token blocks fastest so that consecutive chunks
-// extend the same output rows. Consumer warp w takes tokens 16*(w%8) .. +15
-// of channels 64*(w/8) .. +63, two adjacent channels per lane: per token one
-// shared-memory read covers 64 contiguous channels. Per-channel partial
-// maxima over the 16 tokens go to the exchange buffer [parity][8][128]; after
-// the barrier each lane reduces the 8 partials of its channels, computes the
-// 128x1 scales and writes each channel's 16 codes as one 16-byte store into
-// the transposed output row. A tile wholly at or beyond the group's valid
-// rows is not loaded: it quantizes to zeros with scale 1.
+// Chunk: one 128-token x 64-channel source tile (E4M3 8 KB plus the 128
+// token scales of its 128-channel block, BF16 16 KB, FP32 32 KB), token
+// blocks fastest so that consecutive chunks extend the same output rows.
+// Two CTAs of 8 consumer warps share an SM, each with half the ring, so two
+// tiles' latency chains overlap. Consumer warp w takes tokens 16w .. 16w+15,
+// two adjacent channels per lane: per token one shared-memory read covers
+// the tile's 64 contiguous channels.
+// Two phases per tile, pipelined across tiles so that the cross-warp wait
+// of one tile overlaps the reads of the next:
+//   A(i): read the tile, reduce this warp's per-channel maxima over its 16
+//         tokens, post them to exchange slot i % 4 and arrive on its barrier;
+//   B(i): read the tile again (the stage is still held), wait until all 8
+//         warps have posted tile i, reduce the 8 partials of each channel,
+//         compute the 128x1 scales, quantize, write each channel's 16 codes
+//         as one 16-byte store into the transposed output row, and release
+//         the stage.
+// A warp runs A(i+1) before B(i). Four exchange slots make the reuse safe:
+// a warp can only post tile i+4 after B(i+2), which needs every warp's
+// A(i+2), which each warp runs after its B(i).
+// A tile wholly at or beyond the group's valid rows is not loaded: it
+// quantizes to zeros with scale 1.
 template <int kSrc>  // 0: E4M3 + 1x128 scales, 1: BF16, 2: FP32
 struct Requant128x1 {
+  static constexpr int kCh = 64;  // channels per tile
+  static constexpr int kWarps = 8, kCtasPerSm = 2;
   static constexpr int kEsz = kSrc == 0 ? 1 : (kSrc == 1 ? 2 : 4);
-  static constexpr int kTileBytes = kTile * kTile * kEsz;
-  // an E4M3 tile carries its 128 token scales (512 B) behind it
+  static constexpr int kTileBytes = kTile * kCh * kEsz;
+  // an E4M3 tile carries the 128 token scales (512 B) of its channel block
   static constexpr int kStageBytes = kTileBytes + (kSrc == 0 ? kTile * 4 : 0);
-  static constexpr int kBoxRows = kSrc == 2 ? 64 : 128;
-  static constexpr int kStages = kRingBytes / kStageBytes;
-  static constexpr int kRedBytes = 2 * 8 * kTile * 4;
+  static constexpr int kStages = kRingBytes / kCtasPerSm / kStageBytes;
+  static constexpr int kSlots = 4;
+  static constexpr int kExchBars = kSlots;
+  static constexpr int kRedBytes = kSlots * kWarps * kCh * 4;
   // rows past the valid count are +0; stored negated that is (-0, -0)
   static constexpr uint64_t kNegZero2 = 0x8000000080000000ull;
 
   struct Args {
     int64_t chunks, T, C, ld_t, ld_c;
-    int TB, CB;
+    int TB, CB;  // 128-token blocks, 64-channel blocks
     const float* s_src;
     const int32_t* valid_rows;
     uint8_t* qT;
@@ -417,7 +455,15 @@ struct Requant128x1 {
     int pow2;
   };
 
-  // d2 = group, d1 = 128-channel block, d0 = 128-token block
+  // the tile of phase A waiting for its phase B
+  struct State {
+    bool has;
+    Slot sl;
+    int64_t g;
+    int cb, tb;
+  };
+
+  // d2 = group, d1 = 64-channel block, d0 = 128-token block
   static __device__ __forceinline__ void walk_init(const Args& a, Walk& w, int64_t c, int64_t step) {
     w.init(c, step, a.CB, a.TB);
   }
@@ -433,76 +479,93 @@ struct Requant128x1 {
       return;
     }
     mbar_arrive_expect_tx(full, kStageBytes);
-#pragma unroll
-    for (int i = 0; i < kTile / kBoxRows; ++i)
-      tma_load_3d(dst + i * kBoxRows * kTile * kEsz, &tm, full, w.d1 * kTile, w.d0 * kTile + i * kBoxRows,
-                  static_cast<int32_t>(w.d2));
+    tma_load_3d(dst, &tm, full, w.d1 * kCh, w.d0 * kTile, static_cast<int32_t>(w.d2));
     if constexpr (kSrc == 0)
-      bulk_load(dst + kTileBytes, a.s_src + (w.d2 * a.CB + w.d1) * a.ld_t + static_cast<int64_t>(w.d0) * kTile,
-                kTile * 4, full);
+      bulk_load(dst + kTileBytes,
+                a.s_src + (w.d2 * (a.CB / 2) + w.d1 / 2) * a.ld_t + static_cast<int64_t>(w.d0) * kTile, kTile * 4,
+                full);
   }
 
-  static __device__ __forceinline__ bool consume(const Args& a, const Pipe& p, const Walk& w, const Slot& sl,
-                                                 int cw, int lane) {
-    const int64_t g = w.d2;
-    const int tg = cw & 7, chh = cw >> 3;
-    const int c0 = chh * 64 + 2 * lane;  // this lane's first channel within the tile
-    const int64_t tile_t0 = static_cast<int64_t>(w.d0) * kTile;
-    const int64_t t0 = tile_t0 + tg * 16;
-    const int64_t valid = valid_of(a, g);
-    const bool live = tile_t0 < valid;  // the tile has at least one valid row
-    if (!wait_full(sl, p)) return false;
-
-    // x[k] = (-x[t0+k][c0], -x[t0+k][c0+1]) as an f32 pair
-    uint64_t x[16];
-    if (live) {
+  // This lane's 16 tokens x 2 channels, negated, as f32 pairs (token k of
+  // the warp's group in x[k]); rows past `valid` read as +0.
+  static __device__ __forceinline__ void load_tile(const uint8_t* st, int tg, int c0, int64_t t0, int64_t valid,
+                                                   uint64_t (&x)[16]) {
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const int t = tg * 16 + k;
-        if constexpr (kSrc == 0) {
-          const uint32_t b = *reinterpret_cast<const uint16_t*>(sl.st + t * kTile + c0);
-          const float2 f = e4m3x2_to_f32(b);
-          const float nts = -reinterpret_cast<const float*>(sl.st + kTileBytes)[t];  // token scale, negated
-          x[k] = mul2(pk2(f.x, f.y), pk2(nts, nts));
-        } else if constexpr (kSrc == 1) {
-          x[k] = neg_bf16x2(*reinterpret_cast<const uint32_t*>(sl.st + (t * kTile + c0) * 2));
-        } else {
-          const float2 f = *reinterpret_cast<const float2*>(sl.st + (t * kTile + c0) * 4);
-          x[k] = pk2(-f.x, -f.y);
-        }
+    for (int k = 0; k < 16; ++k) {
+      const int t = tg * 16 + k;
+      if constexpr (kSrc == 0) {
+        const uint32_t b = *reinterpret_cast<const uint16_t*>(st + t * kCh + c0);
+        const float2 f = e4m3x2_to_f32(b);
+        const float nts = -reinterpret_cast<const float*>(st + kTileBytes)[t];  // token scale, negated
+        x[k] = mul2(pk2(f.x, f.y), pk2(nts, nts));
+      } else if constexpr (kSrc == 1) {
+        x[k] = neg_bf16x2(*reinterpret_cast<const uint32_t*>(st + (t * kCh + c0) * 2));
+      } else {
+        const float2 f = *reinterpret_cast<const float2*>(st + (t * kCh + c0) * 4);
+        x[k] = pk2(-f.x, -f.y);
       }
     }
-    float a0 = 0.0f, a1 = 0.0f;
-    if (live) {
-      if (t0 + 16 > valid) {  // the tile straddles the group's last valid row
+    if (t0 + 16 > valid) {  // the tile straddles the group's last valid row
 #pragma unroll
-        for (int k = 0; k < 16; ++k)
-          if (t0 + k >= valid) x[k] = kNegZero2;
-      }
+      for (int k = 0; k < 16; ++k)
+        if (t0 + k >= valid) x[k] = kNegZero2;
+    }
+  }
+
+  static __device__ __forceinline__ bool phase_a(const Args& a, const Pipe& p, int64_t g, int tb, const Slot& sl,
+                                                 int cw, int lane) {
+    const int tg = cw, c0 = 2 * lane;
+    const int64_t tile_t0 = static_cast<int64_t>(tb) * kTile;
+    const int64_t valid = valid_of(a, g);
+    if (!wait_full(sl, p)) return false;
+    float a0 = 0.0f, a1 = 0.0f;
+    if (tile_t0 < valid) {
+      uint64_t x[16];
+      load_tile(stage_of(sl), tg, c0, tile_t0 + tg * 16, valid, x);
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
         const float2 f = unpk2(x[k]);
         a0 = fmaxf(a0, fabsf(f.x));
         a1 = fmaxf(a1, fabsf(f.y));
       }
+    }
+    float* rb = red_of(sl) + (sl.it % kSlots) * kWarps * kCh;
+    *reinterpret_cast<float2*>(rb + tg * kCh + c0) = make_float2(a0, a1);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sl.red_bar + (sl.it % kSlots) * 8);
+    return true;
+  }
+
+  static __device__ __forceinline__ bool phase_b(const Args& a, const Pipe& p, int64_t g, int cb, int tb,
+                                                 const Slot& sl, int cw, int lane) {
+    const int tg = cw, c0 = 2 * lane;
+    const int64_t tile_t0 = static_cast<int64_t>(tb) * kTile;
+    const int64_t t0 = tile_t0 + tg * 16;
+    const int64_t valid = valid_of(a, g);
+    // read the tile again first: its latency overlaps the exchange wait
+    uint64_t x[16];
+    if (tile_t0 < valid) {
+      load_tile(stage_of(sl), tg, c0, t0, valid, x);
     } else {
 #pragma unroll
       for (int k = 0; k < 16; ++k) x[k] = kNegZero2;
     }
+    if (!mbar_wait_sleep(sl.red_bar + (sl.it % kSlots) * 8, (sl.it / kSlots) & 1, p.status,
+                         kStatusTimeoutQuantConsumer, p.wait_limit_ns))
+      return false;
     release(sl, lane);
-    float* rb = sl.red + (sl.it & 1) * 8 * kTile;
-    *reinterpret_cast<float2*>(rb + tg * kTile + c0) = make_float2(a0, a1);
-    if (!exchange(sl, p, lane)) return false;
+    const float* rb = red_of(sl) + (sl.it % kSlots) * kWarps * kCh;
+    float a0 = 0.0f, a1 = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float2 t = *reinterpret_cast<const float2*>(rb + i * kTile + c0);
+    for (int i = 0; i < kWarps; ++i) {
+      const float2 t = *reinterpret_cast<const float2*>(rb + i * kCh + c0);
       a0 = fmaxf(a0, t.x);
       a1 = fmaxf(a1, t.y);
     }
     const float s0 = tile_scale(a0, a.pow2 != 0), s1 = tile_scale(a1, a.pow2 != 0);
-    const int64_t ch = static_cast<int64_t>(w.d1) * kTile + c0;  // channel index within the group
+    const int64_t ch = static_cast<int64_t>(cb) * kCh + c0;  // channel index within the group
     if (tg == 0) {
-      float* sr = a.sT + (g * a.TB + w.d0) * a.ld_c + ch;
+      float* sr = a.sT + (g * a.TB + tb) * a.ld_c + ch;
       sr[0] = s0;
       sr[1] = s1;
     }
@@ -538,6 +601,22 @@ struct Requant128x1 {
     *reinterpret_cast<uint4*>(row0 + a.T) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
     return true;
   }
+
+  static __device__ __forceinline__ bool consume(const Args& a, const Pipe& p, const Walk& w, const Slot& sl,
+                                                 int cw, int lane, State& st) {
+    if (!phase_a(a, p, w.d2, w.d0, sl, cw, lane)) return false;
+    if (st.has && !phase_b(a, p, st.g, st.cb, st.tb, st.sl, cw, lane)) return false;
+    st.has = true;
+    st.sl = sl;
+    st.g = w.d2;
+    st.cb = w.d1;
+    st.tb = w.d0;
+    return true;
+  }
+
+  static __device__ __forceinline__ void finish(const Args& a, const Pipe& p, int cw, int lane, State& st) {
+    if (st.has) phase_b(a, p, st.g, st.cb, st.tb, st.sl, cw, lane);
+  }
 };
 
 // ---------------------------------------------------------------- host side
@@ -561,8 +640,9 @@ cudaError_t launch_pipe(const CUtensorMap& tm, const typename Op::Args& a, const
   static_assert(Layout<Op>::kSmem <= 227 * 1024, "shared memory budget");
   cudaError_t e = ensure_attr<Op>();
   if (e != cudaSuccess) return e;
-  const int64_t grid = a.chunks < num_sms ? a.chunks : num_sms;
-  quant_pipe_kernel<Op><<<static_cast<unsigned>(grid), kThreads, Layout<Op>::kSmem, stream>>>(tm, a, p);
+  const int64_t ctas = static_cast<int64_t>(num_sms) * Op::kCtasPerSm;
+  const int64_t grid = a.chunks < ctas ? a.chunks : ctas;
+  quant_pipe_kernel<Op><<<static_cast<unsigned>(grid), 32 * (1 + Op::kWarps), Layout<Op>::kSmem, stream>>>(tm, a, p);
   return cudaGetLastError();
 }
 
@@ -616,12 +696,11 @@ cudaError_t launch_requant_128x1(const void* src, int src_kind, const float* s_s
                                  int64_t T, int64_t C, const int32_t* valid_rows, uint8_t* qT, float* sT,
                                  int64_t ld_c, int pow2, const QuantLaunch& l, cudaStream_t stream) {
   const int esz = src_kind == 0 ? 1 : (src_kind == 1 ? 2 : 4);
-  const int box_rows = src_kind == 2 ? Requant128x1<2>::kBoxRows : kTile;
-  const int64_t TB = T / kTile, CB = C / kTile;
+  constexpr int kCh = Requant128x1<0>::kCh;
+  const int64_t TB = T / kTile, CB = C / kCh;
   if (TB > kMaxBlocks || CB > kMaxBlocks) return cudaErrorInvalidValue;
   CUtensorMap tm;
-  if (!make_map(&tm, map_type(esz), src, C, T, G, C * esz, T * C * esz, kTile, box_rows,
-                CU_TENSOR_MAP_SWIZZLE_NONE))
+  if (!make_map(&tm, map_type(esz), src, C, T, G, C * esz, T * C * esz, kCh, kTile, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   const Pipe p{l.status, l.wait_limit_ns, l.debug_skip_fill};
   const int tb = static_cast<int>(TB), cb = static_cast<int>(CB);
