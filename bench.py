@@ -444,7 +444,7 @@ def run_case(args):
     wgrad E,T,N,C     masked-K weight gradient dW_e = G_e^T X_e (128x1 pow2 operands, FP32 out)
     quant1x128 M,K    activation quantization of bf16 [M, K]
     quant128x128 N,K  weight quantization of bf16 [N, K]
-    requant T,C       128x1 requantization of an E4M3 [T, C] with 1x128 scales (pow2)
+    requant T,C       128x1 requantization (pow2) of [T, C]: E4M3 with 1x128 scales, or --src bf16/fp32
     """
     import torch
     import fp8_fine_grained_24_b300 as fg
@@ -519,11 +519,17 @@ def run_case(args):
             return lambda: fg.fp8_quant_128x128_out(w, q, s), quant_128x128_bytes(N, K), None
         if args.case == "requant":
             T, C = dims
-            qa, sa = fg.fp8_quant_1x128(wl.activations(T, C, seed, device=dev))
+            x = wl.activations(T, C, seed, device=dev)
             qT = torch.empty((C, T), dtype=torch.uint8, device=dev)
             sT = torch.empty((T // 128, fg.scale_ld(C)), dtype=torch.float32, device=dev)
-            return (lambda: fg.fp8_requant_128x1_out(qa.view(torch.float8_e4m3fn), sa, qT, sT, pow2=True),
-                    T * C * 2 + T * (C // 128) * 4 + (T // 128) * C * 4, None)
+            out_bytes = T * C + (T // 128) * C * 4
+            if args.src == "e4m3":
+                qa, sa = fg.fp8_quant_1x128(x)
+                return (lambda: fg.fp8_requant_128x1_out(qa.view(torch.float8_e4m3fn), sa, qT, sT, pow2=True),
+                        T * C + T * (C // 128) * 4 + out_bytes, None)
+            xs = x if args.src == "bf16" else x.float()
+            return (lambda: fg.fp8_requant_128x1_out(xs, None, qT, sT, pow2=True),
+                    T * C * xs.element_size() + out_bytes, None)
         raise SystemExit(f"unknown case {args.case}")
 
     # Independent buffer sets, called round robin, so that the working set
@@ -578,6 +584,8 @@ def run_case(args):
 
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--src", choices=["e4m3", "bf16", "fp32"], default="e4m3",
+                    help="requant case: source type (E4M3 with 1x128 scales, BF16 or FP32)")
     ap.add_argument("--case", choices=["gemm", "contig", "masked", "wgrad", "quant1x128", "quant128x128", "requant"],
                     default=None,
                     help="time a single kernel on --shape instead of the full step")

@@ -114,13 +114,18 @@ __device__ __forceinline__ uint2 codes8(const uint64_t (&v)[4]) {
 }
 
 // ---------------------------------------------------------------- pipeline
-// Shared memory: kStages stages of kStageBytes, then full[S], empty[S] and
-// Op::kExchBars exchange barriers (8 bytes each), then the exchange buffer.
+// Shared memory: Op::kOutBytes of output staging (1024-byte aligned, for
+// swizzled TMA stores), kStages stages of kStageBytes, then full[S],
+// empty[S] and Op::kExchBars exchange barriers (8 bytes each), then the
+// exchange buffer.
 template <class Op>
 struct Layout {
-  static constexpr int kBarOff = Op::kStages * Op::kStageBytes;
+  static_assert(Op::kOutBytes % 1024 == 0, "output staging keeps the stages 1024-byte aligned");
+  static constexpr int kStageOff = Op::kOutBytes;
+  static constexpr int kBarOff = kStageOff + Op::kStages * Op::kStageBytes;
   static constexpr int kRedOff = (kBarOff + (2 * Op::kStages + Op::kExchBars) * 8 + 15) / 16 * 16;
-  static constexpr int kSmem = kRedOff + Op::kRedBytes;
+  // + slack to align the output staging to 1024 bytes at run time
+  static constexpr int kSmem = kRedOff + Op::kRedBytes + (Op::kOutBytes ? 1024 : 0);
 };
 
 // The pipeline's dynamic shared memory. Stages and the exchange buffer are
@@ -129,28 +134,35 @@ struct Layout {
 // rather than a generic one.
 extern __shared__ __align__(1024) uint8_t quant_smem[];
 
-// Per-chunk context handed to a consumer.
+// Per-chunk context handed to a consumer. Offsets are bytes from quant_smem;
+// the layout starts `off` bytes in (1024-byte alignment of the output
+// staging, 0 for ops without it).
 struct Slot {
-  uint32_t st_off;  // the stage: byte offset in quant_smem
+  uint32_t off;
+  uint32_t st_off;  // the stage
   uint32_t full, empty, ph;
   uint32_t red_bar;
-  uint32_t red_off;  // the exchange buffer: byte offset in quant_smem
+  uint32_t red_off;  // the exchange buffer
   uint32_t it;       // this CTA's chunk counter (exchange-buffer parity)
+  const CUtensorMap* tmo;  // output tensor map (ops that store through TMA)
 };
 
 __device__ __forceinline__ const uint8_t* stage_of(const Slot& sl) { return quant_smem + sl.st_off; }
 __device__ __forceinline__ float* red_of(const Slot& sl) { return reinterpret_cast<float*>(quant_smem + sl.red_off); }
 
-// Warp 0 lane 0 fills stages; warps 1..Op::kWarps consume them in the same
-// chunk order (chunk c = blockIdx.x + i * gridDim.x). Op::kCtasPerSm CTAs
-// share an SM.
+// Warp 0 lane 0 fills stages in chunk order (chunk c = blockIdx.x +
+// i * gridDim.x); warps 1..Op::kWarps consume them, in Op::kTeams teams of
+// Op::kTeamWarps warps, team t taking chunks i = t mod kTeams. Op::kCtasPerSm
+// CTAs share an SM.
 template <class Op>
 __global__ void __launch_bounds__(32 * (1 + Op::kWarps), Op::kCtasPerSm)
-    quant_pipe_kernel(const __grid_constant__ CUtensorMap tm, const typename Op::Args a, const Pipe p) {
-  uint8_t* const smem = quant_smem;
+    quant_pipe_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tmo,
+                      const typename Op::Args a, const Pipe p) {
   constexpr int S = Op::kStages;
   using L = Layout<Op>;
-  const uint32_t base = smem_u32(smem);
+  const uint32_t raw = smem_u32(quant_smem);
+  const uint32_t off = Op::kOutBytes ? ((1024u - (raw & 1023u)) & 1023u) : 0u;
+  const uint32_t base = raw + off;
   const uint32_t bar0 = base + L::kBarOff;
   const uint32_t red_bar = bar0 + 2 * S * 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -159,7 +171,7 @@ __global__ void __launch_bounds__(32 * (1 + Op::kWarps), Op::kCtasPerSm)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(bar0 + s * 8, 1);
-      mbar_init(bar0 + (S + s) * 8, Op::kWarps);
+      mbar_init(bar0 + (S + s) * 8, Op::kReleasers);
     }
     for (int i = 0; i < Op::kExchBars; ++i) mbar_init(red_bar + i * 8, Op::kWarps);
     fence_barrier_init();
@@ -176,7 +188,7 @@ __global__ void __launch_bounds__(32 * (1 + Op::kWarps), Op::kCtasPerSm)
         if (!mbar_wait_sleep(bar0 + (S + s) * 8, ph ^ 1, p.status, kStatusTimeoutQuantProducer, p.wait_limit_ns))
           break;
         if (static_cast<int>(it) != p.debug_skip_fill)  // test hook: a fill that never lands
-          Op::issue(tm, a, w, base + s * Op::kStageBytes, bar0 + s * 8);
+          Op::issue(tm, a, w, base + L::kStageOff + s * Op::kStageBytes, bar0 + s * 8);
         if (++s == S) {
           s = 0;
           ph ^= 1;
@@ -195,20 +207,30 @@ __global__ void __launch_bounds__(32 * (1 + Op::kWarps), Op::kCtasPerSm)
   }
 
   const int cw = warp - 1;
+  const int team = Op::kTeams > 1 ? cw / Op::kTeamWarps : 0;
+  if (Op::kTeams > 1) {
+    Op::walk_init(a, w, static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(team) * gridDim.x,
+                  static_cast<int64_t>(Op::kTeams) * gridDim.x);
+    it = s = team;
+  }
   typename Op::State state{};
   bool ok = true;
-  for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x, ++it, w.advance()) {
-    const Slot sl{s * Op::kStageBytes, bar0 + s * 8, bar0 + (S + s) * 8, ph, red_bar, L::kRedOff, it};
+  for (int64_t c = blockIdx.x + static_cast<int64_t>(team) * gridDim.x; c < chunks;
+       c += static_cast<int64_t>(Op::kTeams) * gridDim.x, it += Op::kTeams, w.advance()) {
+    const Slot sl{off, off + L::kStageOff + s * Op::kStageBytes, bar0 + s * 8, bar0 + (S + s) * 8, ph, red_bar,
+                  off + L::kRedOff, it, &tmo};
     if (!Op::consume(a, p, w, sl, cw, lane, state)) {
       ok = false;
       break;
     }
-    if (++s == S) {
-      s = 0;
+    s += Op::kTeams;
+    if (s >= S) {
+      s -= S;
       ph ^= 1;
     }
   }
   if (ok) Op::finish(a, p, cw, lane, state);
+  if (Op::kOutBytes && lane == 0) bulk_wait_all();  // stores issued by this warp
 }
 
 __device__ __forceinline__ bool wait_full(const Slot& sl, const Pipe& p) {
@@ -250,7 +272,8 @@ struct Quant1x128 {
   static constexpr int kEsz = kF32 ? 4 : 2;
   static constexpr int kRows = kF32 ? 64 : 128;
   static constexpr int kStageBytes = kRows * kTile * kEsz;
-  static constexpr int kWarps = kConsumerWarps, kCtasPerSm = 1;
+  static constexpr int kWarps = kConsumerWarps, kCtasPerSm = 1, kOutBytes = 0, kReleasers = kWarps;
+  static constexpr int kTeams = 1, kTeamWarps = kWarps;
   static constexpr int kStages = kRingBytes / kStageBytes;
   static constexpr int kRedBytes = 0;
   static constexpr int kExchBars = 0;
@@ -337,7 +360,8 @@ struct Quant128x128 {
   static constexpr int kEsz = kF32 ? 4 : 2;
   static constexpr int kStageBytes = kTile * kTile * kEsz;
   static constexpr int kBoxRows = kF32 ? 64 : 128;
-  static constexpr int kWarps = kConsumerWarps, kCtasPerSm = 1;
+  static constexpr int kWarps = kConsumerWarps, kCtasPerSm = 1, kOutBytes = 0, kReleasers = kWarps;
+  static constexpr int kTeams = 1, kTeamWarps = kWarps;
   static constexpr int kStages = kRingBytes / kStageBytes;
   static constexpr int kRedBytes = 2 * kConsumerWarps * 4;
   static constexpr int kExchBars = 1;
@@ -409,61 +433,78 @@ struct Quant128x128 {
 };
 
 // ------------------------------------------------------------ 128x1
-// Chunk: one 128-token x 64-channel source tile (E4M3 8 KB plus the 128
-// token scales of its 128-channel block, BF16 16 KB, FP32 32 KB), token
-// blocks fastest so that consecutive chunks extend the same output rows.
-// Two CTAs of 8 consumer warps share an SM, each with half the ring, so two
-// tiles' latency chains overlap. Consumer warp w takes tokens 16w .. 16w+15,
-// two adjacent channels per lane: per token one shared-memory read covers
-// the tile's 64 contiguous channels.
-// Two phases per tile, pipelined across tiles so that the cross-warp wait
-// of one tile overlaps the reads of the next:
-//   A(i): read the tile, reduce this warp's per-channel maxima over its 16
-//         tokens, post them to exchange slot i % 4 and arrive on its barrier;
-//   B(i): read the tile again (the stage is still held), wait until all 8
-//         warps have posted tile i, reduce the 8 partials of each channel,
-//         compute the 128x1 scales, quantize, write each channel's 16 codes
-//         as one 16-byte store into the transposed output row, and release
-//         the stage.
-// A warp runs A(i+1) before B(i). Four exchange slots make the reuse safe:
-// a warp can only post tile i+4 after B(i+2), which needs every warp's
-// A(i+2), which each warp runs after its B(i).
+// Chunk: one 128-token x 128-channel source tile (E4M3 16 KB plus the 128
+// token scales of its channel block, BF16 32 KB, FP32 64 KB), token blocks
+// fastest so that consecutive chunks extend the same output rows.
+//
+// Each consumer warp owns 16 channels of the tile across all 128 tokens, so
+// a channel's amax is a reduction inside one warp: no warp waits for
+// another, and the values stay in registers from load to store. Lane (m, h)
+// (m = lane / 2, h = lane % 2) holds channels 8h .. 8h+7 of the warp's 16
+// for tokens 8m .. 8m+7: 64 elements.
+//
+// Shared-memory layout. The tile arrives through a rank-4 view of the
+// source, (32-byte column group, token, group, batch), as
+// [group][128 tokens][32 bytes]: a lane's 8 channels of one token are 8, 16
+// or 32 contiguous bytes, and consecutive tokens of a group are 32 bytes
+// apart, so the four tokens t % 4 = 0..3 of one group cover all banks.
+// Lane (m, h) reads its k-th token as 8m + (k ^ (m % 8)): at every read the
+// 16 lanes of one h are spread over the four residues (two-way conflicts
+// for E4M3 and FP32 rows, none for BF16). The output bytes are permuted
+// back (one byte permute per 4 bytes) before the store.
+//
+// Output: each warp writes its 16 channel rows of the transposed tile
+// (16 x 128 codes) into its own 2 KB image in shared memory (128-byte
+// swizzled) and sends it with one TMA store; before it rewrites the image
+// for its next tile it waits until that store has read it.
+//
+// Two teams of 8 consumer warps take alternate tiles (one team for FP32,
+// whose 64 KB stages leave room for few), so that one team's loads and
+// reductions overlap the other's.
+//
 // A tile wholly at or beyond the group's valid rows is not loaded: it
 // quantizes to zeros with scale 1.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t c0, int32_t c1,
+                                            int32_t c2, int32_t c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
 template <int kSrc>  // 0: E4M3 + 1x128 scales, 1: BF16, 2: FP32
 struct Requant128x1 {
-  static constexpr int kCh = 64;  // channels per tile
-  static constexpr int kWarps = 8, kCtasPerSm = 2;
   static constexpr int kEsz = kSrc == 0 ? 1 : (kSrc == 1 ? 2 : 4);
-  static constexpr int kTileBytes = kTile * kCh * kEsz;
-  // an E4M3 tile carries the 128 token scales (512 B) of its channel block
+  static constexpr int kTeams = kSrc == 2 ? 1 : 2;
+  static constexpr int kTeamWarps = 8;  // 8 x 16 channels
+  static constexpr int kWarps = kTeams * kTeamWarps, kCtasPerSm = 1;
+  static constexpr int kReleasers = kTeamWarps;  // one team reads each stage
+  static constexpr int kRow = 32;                // bytes of a token row in one column group
+  static constexpr int kGroupBytes = kTile * kRow;
+  static constexpr int kTileBytes = kTile * kTile * kEsz;
+  // an E4M3 tile carries its 128 token scales (512 B)
   static constexpr int kStageBytes = kTileBytes + (kSrc == 0 ? kTile * 4 : 0);
-  static constexpr int kStages = kRingBytes / kCtasPerSm / kStageBytes;
-  static constexpr int kSlots = 4;
-  static constexpr int kExchBars = kSlots;
-  static constexpr int kRedBytes = kSlots * kWarps * kCh * 4;
+  static constexpr int kImageBytes = 16 * kTile;  // a warp's 16 channel rows
+  static constexpr int kOutBytes = kWarps * kImageBytes;
+  static constexpr int kExchBars = 0, kRedBytes = 0;
+  static constexpr int kStages = (227 * 1024 - 1024 - kOutBytes - 512) / kStageBytes;
+  static_assert(kStages >= 2 * kTeams, "ring depth");
   // rows past the valid count are +0; stored negated that is (-0, -0)
   static constexpr uint64_t kNegZero2 = 0x8000000080000000ull;
 
   struct Args {
     int64_t chunks, T, C, ld_t, ld_c;
-    int TB, CB;  // 128-token blocks, 64-channel blocks
+    int TB, CB;  // 128-token blocks, 128-channel blocks
     const float* s_src;
     const int32_t* valid_rows;
-    uint8_t* qT;
     float* sT;
     int pow2;
   };
 
-  // the tile of phase A waiting for its phase B
-  struct State {
-    bool has;
-    Slot sl;
-    int64_t g;
-    int cb, tb;
-  };
+  struct State {};
 
-  // d2 = group, d1 = 64-channel block, d0 = 128-token block
+  // d2 = group, d1 = 128-channel block, d0 = 128-token block
   static __device__ __forceinline__ void walk_init(const Args& a, Walk& w, int64_t c, int64_t step) {
     w.init(c, step, a.CB, a.TB);
   }
@@ -479,144 +520,174 @@ struct Requant128x1 {
       return;
     }
     mbar_arrive_expect_tx(full, kStageBytes);
-    tma_load_3d(dst, &tm, full, w.d1 * kCh, w.d0 * kTile, static_cast<int32_t>(w.d2));
+    tma_load_4d(dst, &tm, full, 0, w.d0 * kTile, w.d1 * (kTile * kEsz / kRow), static_cast<int32_t>(w.d2));
     if constexpr (kSrc == 0)
-      bulk_load(dst + kTileBytes,
-                a.s_src + (w.d2 * (a.CB / 2) + w.d1 / 2) * a.ld_t + static_cast<int64_t>(w.d0) * kTile, kTile * 4,
-                full);
+      bulk_load(dst + kTileBytes, a.s_src + (w.d2 * a.CB + w.d1) * a.ld_t + static_cast<int64_t>(w.d0) * kTile,
+                kTile * 4, full);
   }
 
-  // This lane's 16 tokens x 2 channels, negated, as f32 pairs (token k of
-  // the warp's group in x[k]); rows past `valid` read as +0.
-  static __device__ __forceinline__ void load_tile(const uint8_t* st, int tg, int c0, int64_t t0, int64_t valid,
-                                                   uint64_t (&x)[16]) {
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const int t = tg * 16 + k;
-      if constexpr (kSrc == 0) {
-        const uint32_t b = *reinterpret_cast<const uint16_t*>(st + t * kCh + c0);
-        const float2 f = e4m3x2_to_f32(b);
-        const float nts = -reinterpret_cast<const float*>(st + kTileBytes)[t];  // token scale, negated
-        x[k] = mul2(pk2(f.x, f.y), pk2(nts, nts));
-      } else if constexpr (kSrc == 1) {
-        x[k] = neg_bf16x2(*reinterpret_cast<const uint32_t*>(st + (t * kCh + c0) * 2));
-      } else {
-        const float2 f = *reinterpret_cast<const float2*>(st + (t * kCh + c0) * 4);
-        x[k] = pk2(-f.x, -f.y);
-      }
-    }
-    if (t0 + 16 > valid) {  // the tile straddles the group's last valid row
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        if (t0 + k >= valid) x[k] = kNegZero2;
-    }
-  }
-
-  static __device__ __forceinline__ bool phase_a(const Args& a, const Pipe& p, int64_t g, int tb, const Slot& sl,
-                                                 int cw, int lane) {
-    const int tg = cw, c0 = 2 * lane;
-    const int64_t tile_t0 = static_cast<int64_t>(tb) * kTile;
-    const int64_t valid = valid_of(a, g);
-    if (!wait_full(sl, p)) return false;
-    float a0 = 0.0f, a1 = 0.0f;
-    if (tile_t0 < valid) {
-      uint64_t x[16];
-      load_tile(stage_of(sl), tg, c0, tile_t0 + tg * 16, valid, x);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float2 f = unpk2(x[k]);
-        a0 = fmaxf(a0, fabsf(f.x));
-        a1 = fmaxf(a1, fabsf(f.y));
-      }
-    }
-    float* rb = red_of(sl) + (sl.it % kSlots) * kWarps * kCh;
-    *reinterpret_cast<float2*>(rb + tg * kCh + c0) = make_float2(a0, a1);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(sl.red_bar + (sl.it % kSlots) * 8);
-    return true;
-  }
-
-  static __device__ __forceinline__ bool phase_b(const Args& a, const Pipe& p, int64_t g, int cb, int tb,
-                                                 const Slot& sl, int cw, int lane) {
-    const int tg = cw, c0 = 2 * lane;
-    const int64_t tile_t0 = static_cast<int64_t>(tb) * kTile;
-    const int64_t t0 = tile_t0 + tg * 16;
-    const int64_t valid = valid_of(a, g);
-    // read the tile again first: its latency overlaps the exchange wait
-    uint64_t x[16];
-    if (tile_t0 < valid) {
-      load_tile(stage_of(sl), tg, c0, t0, valid, x);
+  // The lane's 8 channels of token t, negated, as 4 f32 pairs.
+  static __device__ __forceinline__ void load_token(const uint8_t* src, int t, float ts, uint64_t (&v)[4]) {
+    const uint8_t* p = src + t * kRow;
+    if constexpr (kSrc == 0) {
+      const uint2 w = *reinterpret_cast<const uint2*>(p);
+      const uint64_t ns = pk2(-ts, -ts);
+      v[0] = mul2(e4m3x2_lo_pk(w.x), ns);
+      v[1] = mul2(e4m3x2_hi_pk(w.x), ns);
+      v[2] = mul2(e4m3x2_lo_pk(w.y), ns);
+      v[3] = mul2(e4m3x2_hi_pk(w.y), ns);
+    } else if constexpr (kSrc == 1) {
+      const uint4 w = *reinterpret_cast<const uint4*>(p);
+      v[0] = neg_bf16x2(w.x);
+      v[1] = neg_bf16x2(w.y);
+      v[2] = neg_bf16x2(w.z);
+      v[3] = neg_bf16x2(w.w);
     } else {
-#pragma unroll
-      for (int k = 0; k < 16; ++k) x[k] = kNegZero2;
+      const float4 a = *reinterpret_cast<const float4*>(p);
+      const float4 b = *reinterpret_cast<const float4*>(p + 16);
+      v[0] = pk2(-a.x, -a.y);
+      v[1] = pk2(-a.z, -a.w);
+      v[2] = pk2(-b.x, -b.y);
+      v[3] = pk2(-b.z, -b.w);
     }
-    if (!mbar_wait_sleep(sl.red_bar + (sl.it % kSlots) * 8, (sl.it / kSlots) & 1, p.status,
-                         kStatusTimeoutQuantConsumer, p.wait_limit_ns))
-      return false;
-    release(sl, lane);
-    const float* rb = red_of(sl) + (sl.it % kSlots) * kWarps * kCh;
-    float a0 = 0.0f, a1 = 0.0f;
+  }
+
+  // One step of the reduce-scatter of N channel maxima over lane bit `bit`:
+  // the lane with the bit clear keeps the first N/2 channels, its partner
+  // the last N/2, each taking the max with what the other sends.
+  template <int N>
+  static __device__ __forceinline__ void reduce_half(float (&v)[8], int lane, int bit) {
+    const bool upper = (lane >> bit) & 1;
 #pragma unroll
-    for (int i = 0; i < kWarps; ++i) {
-      const float2 t = *reinterpret_cast<const float2*>(rb + i * kCh + c0);
-      a0 = fmaxf(a0, t.x);
-      a1 = fmaxf(a1, t.y);
+    for (int i = 0; i < N / 2; ++i) {
+      const float send = upper ? v[i] : v[i + N / 2];
+      const float keep = upper ? v[i + N / 2] : v[i];
+      v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 1 << bit));
     }
-    const float s0 = tile_scale(a0, a.pow2 != 0), s1 = tile_scale(a1, a.pow2 != 0);
-    const int64_t ch = static_cast<int64_t>(cb) * kCh + c0;  // channel index within the group
-    if (tg == 0) {
-      float* sr = a.sT + (g * a.TB + tb) * a.ld_c + ch;
-      sr[0] = s0;
-      sr[1] = s1;
-    }
-    const int m0 = make_tile_div_mode(s0), m1 = make_tile_div_mode(s1);
-    const int path = warp_quot_mode(m0 == kQuotDiv || m1 == kQuotDiv ? kQuotDiv
-                                    : (m0 == kQuotMul && m1 == kQuotMul ? kQuotMul : kQuotFma));
-    // per-lane scale pair (channel c0 in the low half, c0+1 in the high half)
-    const float r0 = __frcp_rn(s0), r1 = __frcp_rn(s1);
-    if (path == kQuotMul) {
-      const uint64_t nr2 = pk2(-r0, -r1);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) x[k] = mul2(x[k], nr2);
-    } else if (path == kQuotFma) {
-      const uint64_t s2 = pk2(s0, s1), nr2 = pk2(-r0, -r1);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) x[k] = quot2_fma(x[k], s2, nr2);
-    } else {
-      const TileDiv d0{s0, r0, m0}, d1{s1, r1, m1};
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float2 f = unpk2(x[k]);
-        x[k] = pk2(tile_quot(-f.x, d0), tile_quot(-f.y, d1));
-      }
-    }
-    // x[k] holds (channel c0, channel c0+1) of token k; gather each channel's
-    // 16 tokens into one 16-byte row segment
-    uint32_t lo[4], hi[4];
-#pragma unroll
-    for (int k4 = 0; k4 < 4; ++k4)
-      e4m3_transpose4(x[4 * k4], x[4 * k4 + 1], x[4 * k4 + 2], x[4 * k4 + 3], lo[k4], hi[k4]);
-    uint8_t* row0 = a.qT + (g * a.C + ch) * a.T + t0;
-    *reinterpret_cast<uint4*>(row0) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    *reinterpret_cast<uint4*>(row0 + a.T) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    return true;
   }
 
   static __device__ __forceinline__ bool consume(const Args& a, const Pipe& p, const Walk& w, const Slot& sl,
-                                                 int cw, int lane, State& st) {
-    if (!phase_a(a, p, w.d2, w.d0, sl, cw, lane)) return false;
-    if (st.has && !phase_b(a, p, st.g, st.cb, st.tb, st.sl, cw, lane)) return false;
-    st.has = true;
-    st.sl = sl;
-    st.g = w.d2;
-    st.cb = w.d1;
-    st.tb = w.d0;
+                                                 int cw, int lane, State&) {
+    const int wt = cw % kTeamWarps;           // the warp's 16 channels: 16 wt .. 16 wt + 15
+    const int m = lane >> 1, h = lane & 1;    // tokens 8m .. 8m+7, channels 8h .. 8h+7
+    const int c0 = 16 * wt + 8 * h;           // first channel of the lane in the tile
+    const int64_t g = w.d2;
+    const int cb = w.d1, tb = w.d0;
+    const int64_t nvalid = valid_of(a, g) - static_cast<int64_t>(tb) * kTile;  // valid tokens of the tile
+
+    if (!wait_full(sl, p)) return false;
+    const int m7 = m & 7;
+    uint64_t x[8][4];  // x[k][j]: token 8m + (k ^ m7), channels c0 + 2j, c0 + 2j + 1 (negated)
+    if (nvalid > 0) {
+      const uint8_t* src = stage_of(sl) + (c0 * kEsz / kRow) * kGroupBytes + (c0 * kEsz) % kRow + 8 * m * kRow;
+      const float* ts = reinterpret_cast<const float*>(stage_of(sl) + kTileBytes) + 8 * m;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int u = k ^ m7;
+        load_token(src, u, kSrc == 0 ? ts[u] : 1.0f, x[k]);
+      }
+      if (nvalid < kTile) {  // the tile straddles the group's last valid row
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (8 * m + (k ^ m7) >= nvalid) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) x[k][j] = kNegZero2;
+          }
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[k][j] = kNegZero2;
+    }
+    release(sl, lane);
+
+    // amax of each of the lane's 8 channels over its 8 tokens, then over the
+    // 16 lanes of the same h: after the reduce-scatter lane (m, h) holds
+    // channel c0 + j, j = 4 m3 + 2 m2 + m1 (m = 8 m3 + 4 m2 + 2 m1 + m0).
+    float am[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float e = 0.0f, o = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float2 f = unpk2(x[k][j]);
+        e = fmaxf(e, fabsf(f.x));
+        o = fmaxf(o, fabsf(f.y));
+      }
+      am[2 * j] = e;
+      am[2 * j + 1] = o;
+    }
+    reduce_half<8>(am, lane, 4);
+    reduce_half<4>(am, lane, 3);
+    reduce_half<2>(am, lane, 2);
+    am[0] = fmaxf(am[0], __shfl_xor_sync(0xffffffffu, am[0], 2));
+    const int jm = 4 * ((m >> 3) & 1) + 2 * ((m >> 2) & 1) + ((m >> 1) & 1);
+    const float s = tile_scale(am[0], a.pow2 != 0);
+    const float r = __frcp_rn(s);
+    if ((m & 1) == 0)
+      a.sT[(g * a.TB + tb) * a.ld_c + static_cast<int64_t>(cb) * kTile + c0 + jm] = s;
+    const int path = warp_quot_mode(make_tile_div_mode(s));
+
+    // Per channel pair (2j, 2j+1): the scales from the lanes that hold them
+    // (channel c0 + i sits in lane h + 2 (8 i2 + 4 i1 + 2 i0), i = 4 i2 +
+    // 2 i1 + i0), the quotients, then the codes: channel c0 + i, 8 tokens ->
+    // 8 bytes, byte k for token 8m + (k ^ m7); byte permutes put token
+    // 8m + p in byte p (p ^ m7 selects it). Image row 8h + i, bytes
+    // 8m .. 8m+7 (128-byte swizzle: 16-byte chunk m/2 of row r at chunk
+    // (m/2) ^ (r % 8)).
+    const uint32_t img = sl.off + cw * kImageBytes;
+    if (lane == 0) bulk_wait_read_all();  // the previous image of this warp has been read
+    __syncwarp();
+    const uint32_t sel_lo = 0x3210u ^ (static_cast<uint32_t>(m7) * 0x1111u);
+    const uint32_t sel_hi = 0x7654u ^ (static_cast<uint32_t>(m7) * 0x1111u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i0 = 2 * j, i1 = 2 * j + 1;
+      const int l0 = h + 2 * (8 * ((i0 >> 2) & 1) + 4 * ((i0 >> 1) & 1) + 2 * (i0 & 1));
+      const int l1 = h + 2 * (8 * ((i1 >> 2) & 1) + 4 * ((i1 >> 1) & 1) + 2 * (i1 & 1));
+      const float ra = __shfl_sync(0xffffffffu, r, l0), rb = __shfl_sync(0xffffffffu, r, l1);
+      if (path == kQuotMul) {
+        const uint64_t nr2 = pk2(-ra, -rb);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k][j] = mul2(x[k][j], nr2);
+      } else {
+        const float sa = __shfl_sync(0xffffffffu, s, l0), sb = __shfl_sync(0xffffffffu, s, l1);
+        if (path == kQuotFma) {
+          const uint64_t s2 = pk2(sa, sb), nr2 = pk2(-ra, -rb);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) x[k][j] = quot2_fma(x[k][j], s2, nr2);
+        } else {
+          const TileDiv d0{sa, ra, make_tile_div_mode(sa)}, d1{sb, rb, make_tile_div_mode(sb)};
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float2 f = unpk2(x[k][j]);
+            x[k][j] = pk2(tile_quot(-f.x, d0), tile_quot(-f.y, d1));
+          }
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float q[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) q[k] = e ? unpk2(x[k][j]).y : unpk2(x[k][j]).x;
+        const uint32_t lo = e4m3x4_f(q[0], q[1], q[2], q[3]), hi = e4m3x4_f(q[4], q[5], q[6], q[7]);
+        const uint32_t nlo = __byte_perm(lo, hi, sel_lo), nhi = __byte_perm(lo, hi, sel_hi);
+        const int row = 8 * h + 2 * j + e;
+        const uint32_t off = img + row * kTile + ((((m >> 1) ^ (row & 7)) << 4) | ((m & 1) << 3));
+        *reinterpret_cast<uint2*>(quant_smem + off) = make_uint2(nlo, nhi);
+      }
+    }
+    fence_async_shared();  // the image is read by a TMA store
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(sl.tmo, smem_u32(quant_smem) + img, tb * kTile, cb * kTile + 16 * wt, static_cast<int32_t>(g));
+      bulk_commit();
+    }
     return true;
   }
 
-  static __device__ __forceinline__ void finish(const Args& a, const Pipe& p, int cw, int lane, State& st) {
-    if (st.has) phase_b(a, p, st.g, st.cb, st.tb, st.sl, cw, lane);
-  }
+  static __device__ __forceinline__ void finish(const Args&, const Pipe&, int, int, State&) {}
 };
 
 // ---------------------------------------------------------------- host side
@@ -634,15 +705,19 @@ cudaError_t ensure_attr() {
   return e;
 }
 
+// `tmo` is the output tensor map of ops that store through TMA (others
+// ignore it).
 template <class Op>
-cudaError_t launch_pipe(const CUtensorMap& tm, const typename Op::Args& a, const Pipe& p, int num_sms,
-                        cudaStream_t stream) {
+cudaError_t launch_pipe(const CUtensorMap& tm, const CUtensorMap& tmo, const typename Op::Args& a, const Pipe& p,
+                        int num_sms, cudaStream_t stream) {
   static_assert(Layout<Op>::kSmem <= 227 * 1024, "shared memory budget");
+  // 228 KB per SM, 1 KB of it reserved per CTA
+  static_assert(Op::kCtasPerSm * (Layout<Op>::kSmem + 1024) <= 228 * 1024, "CTAs per SM");
   cudaError_t e = ensure_attr<Op>();
   if (e != cudaSuccess) return e;
   const int64_t ctas = static_cast<int64_t>(num_sms) * Op::kCtasPerSm;
   const int64_t grid = a.chunks < ctas ? a.chunks : ctas;
-  quant_pipe_kernel<Op><<<static_cast<unsigned>(grid), 32 * (1 + Op::kWarps), Layout<Op>::kSmem, stream>>>(tm, a, p);
+  quant_pipe_kernel<Op><<<static_cast<unsigned>(grid), 32 * (1 + Op::kWarps), Layout<Op>::kSmem, stream>>>(tm, tmo, a, p);
   return cudaGetLastError();
 }
 
@@ -668,10 +743,10 @@ cudaError_t launch_quant_1x128(const void* x, bool f32, int64_t M, int64_t K, in
   const int64_t chunks = ((M + rows - 1) / rows) * KB;
   if (f32) {
     typename Quant1x128<true>::Args a{chunks, M, K, lds, KB, q, s, pow2};
-    return launch_pipe<Quant1x128<true>>(tm, a, p, l.num_sms, stream);
+    return launch_pipe<Quant1x128<true>>(tm, tm, a, p, l.num_sms, stream);
   }
   typename Quant1x128<false>::Args a{chunks, M, K, lds, KB, q, s, pow2};
-  return launch_pipe<Quant1x128<false>>(tm, a, p, l.num_sms, stream);
+  return launch_pipe<Quant1x128<false>>(tm, tm, a, p, l.num_sms, stream);
 }
 
 cudaError_t launch_quant_128x128(const void* w, bool f32, int64_t G, int64_t N, int64_t K, uint8_t* q, float* s,
@@ -686,36 +761,43 @@ cudaError_t launch_quant_128x128(const void* w, bool f32, int64_t G, int64_t N, 
   const Pipe p{l.status, l.wait_limit_ns, l.debug_skip_fill};
   if (f32) {
     typename Quant128x128<true>::Args a{G * NB * KB, N, K, static_cast<int>(NB), static_cast<int>(KB), q, s, pow2};
-    return launch_pipe<Quant128x128<true>>(tm, a, p, l.num_sms, stream);
+    return launch_pipe<Quant128x128<true>>(tm, tm, a, p, l.num_sms, stream);
   }
   typename Quant128x128<false>::Args a{G * NB * KB, N, K, static_cast<int>(NB), static_cast<int>(KB), q, s, pow2};
-  return launch_pipe<Quant128x128<false>>(tm, a, p, l.num_sms, stream);
+  return launch_pipe<Quant128x128<false>>(tm, tm, a, p, l.num_sms, stream);
 }
 
 cudaError_t launch_requant_128x1(const void* src, int src_kind, const float* s_src, int64_t ld_t, int64_t G,
                                  int64_t T, int64_t C, const int32_t* valid_rows, uint8_t* qT, float* sT,
                                  int64_t ld_c, int pow2, const QuantLaunch& l, cudaStream_t stream) {
   const int esz = src_kind == 0 ? 1 : (src_kind == 1 ? 2 : 4);
-  constexpr int kCh = Requant128x1<0>::kCh;
-  const int64_t TB = T / kTile, CB = C / kCh;
-  if (TB > kMaxBlocks || CB > kMaxBlocks) return cudaErrorInvalidValue;
-  CUtensorMap tm;
-  if (!make_map(&tm, map_type(esz), src, C, T, G, C * esz, T * C * esz, kCh, kTile, CU_TENSOR_MAP_SWIZZLE_NONE))
+  const int64_t TB = T / kTile, CB = C / kTile;
+  if (TB * CB > kMaxBlocks) return cudaErrorInvalidValue;
+  // source as (32-byte column group, token, group, batch); one box is a tile
+  const uint64_t cols = 32 / esz;
+  const uint64_t dims[4] = {cols, static_cast<uint64_t>(T), static_cast<uint64_t>(C) / cols, static_cast<uint64_t>(G)};
+  const uint64_t strides[3] = {static_cast<uint64_t>(C) * esz, 32, static_cast<uint64_t>(T * C) * esz};
+  const uint32_t box[4] = {static_cast<uint32_t>(cols), kTile, static_cast<uint32_t>(kTile / cols), 1};
+  CUtensorMap tm, tmo;
+  if (!make_map4(&tm, map_type(esz), src, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  // qT [G][C][T]: one store box is a warp's 16 channel rows of 128 codes
+  if (!make_map(&tmo, CU_TENSOR_MAP_DATA_TYPE_UINT8, qT, T, C, G, T, C * T, kTile, 16, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   const Pipe p{l.status, l.wait_limit_ns, l.debug_skip_fill};
   const int tb = static_cast<int>(TB), cb = static_cast<int>(CB);
   switch (src_kind) {
     case 0: {
-      typename Requant128x1<0>::Args a{G * TB * CB, T, C, ld_t, ld_c, tb, cb, s_src, valid_rows, qT, sT, pow2};
-      return launch_pipe<Requant128x1<0>>(tm, a, p, l.num_sms, stream);
+      typename Requant128x1<0>::Args a{G * TB * CB, T, C, ld_t, ld_c, tb, cb, s_src, valid_rows, sT, pow2};
+      return launch_pipe<Requant128x1<0>>(tm, tmo, a, p, l.num_sms, stream);
     }
     case 1: {
-      typename Requant128x1<1>::Args a{G * TB * CB, T, C, ld_t, ld_c, tb, cb, nullptr, valid_rows, qT, sT, pow2};
-      return launch_pipe<Requant128x1<1>>(tm, a, p, l.num_sms, stream);
+      typename Requant128x1<1>::Args a{G * TB * CB, T, C, ld_t, ld_c, tb, cb, nullptr, valid_rows, sT, pow2};
+      return launch_pipe<Requant128x1<1>>(tm, tmo, a, p, l.num_sms, stream);
     }
     default: {
-      typename Requant128x1<2>::Args a{G * TB * CB, T, C, ld_t, ld_c, tb, cb, nullptr, valid_rows, qT, sT, pow2};
-      return launch_pipe<Requant128x1<2>>(tm, a, p, l.num_sms, stream);
+      typename Requant128x1<2>::Args a{G * TB * CB, T, C, ld_t, ld_c, tb, cb, nullptr, valid_rows, sT, pow2};
+      return launch_pipe<Requant128x1<2>>(tm, tmo, a, p, l.num_sms, stream);
     }
   }
 }

@@ -247,6 +247,39 @@ __device__ __forceinline__ float2 e4m3x2_to_f32(uint32_t w) {
   return __half22float2(*reinterpret_cast<__half2*>(&h));
 }
 
+// Four floats -> four E4M3 bytes (RNE, satfinite), a in the low byte.
+__device__ __forceinline__ uint32_t e4m3x4_f(float a, float b, float c, float d) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 l, %2, %1;\n\tcvt.rn.satfinite.e4m3x2.f32 h, %4, %3;\n\t"
+      "mov.b32 %0, {l, h};\n\t}"
+      : "=r"(r)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
+  return r;
+}
+
+// The E4M3 pair in the low (lo_pk) or high (hi_pk) half of w -> the two
+// values (exact) as an f32 pair, the lower byte first.
+__device__ __forceinline__ uint64_t e4m3x2_lo_pk(uint32_t w) {
+  uint64_t r;
+  asm("{\n\t.reg .b16 l, h;\n\t.reg .b32 p;\n\t.reg .f32 a, b;\n\t"
+      "mov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 p, l;\n\tmov.b32 {l, h}, p;\n\t"
+      "cvt.f32.f16 a, l;\n\tcvt.f32.f16 b, h;\n\tmov.b64 %0, {a, b};\n\t}"
+      : "=l"(r)
+      : "r"(w));
+  return r;
+}
+
+__device__ __forceinline__ uint64_t e4m3x2_hi_pk(uint32_t w) {
+  uint64_t r;
+  asm("{\n\t.reg .b16 l, h;\n\t.reg .b32 p;\n\t.reg .f32 a, b;\n\t"
+      "mov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 p, h;\n\tmov.b32 {l, h}, p;\n\t"
+      "cvt.f32.f16 a, l;\n\tcvt.f32.f16 b, h;\n\tmov.b64 %0, {a, b};\n\t}"
+      : "=l"(r)
+      : "r"(w));
+  return r;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

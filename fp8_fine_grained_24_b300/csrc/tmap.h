@@ -13,4 +13,11 @@ namespace fp8fg {
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
               uint64_t stride1, uint64_t stride2, uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw);
 
+// Rank 4: dims (dims[0] contiguous), byte strides of dims 1..3, box. A box
+// lands in shared memory densely in dimension order when sw is
+// CU_TENSOR_MAP_SWIZZLE_NONE; with a swizzle, every innermost row takes a
+// whole swizzle span even when it is shorter.
+bool make_map4(CUtensorMap* m, CUtensorMapDataType dt, const void* base, const uint64_t (&dims)[4],
+               const uint64_t (&strides)[3], const uint32_t (&box)[4], CUtensorMapSwizzle sw);
+
 }  // namespace fp8fg
