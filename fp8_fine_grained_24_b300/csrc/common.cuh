@@ -34,6 +34,19 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------- launch order
+// Programmatic dependent launch: kernels are launched so that they may start
+// before the previous kernel on the stream has finished. Every thread calls
+// this after its prologue (barrier set-up, TMEM allocation) and before its
+// first global-memory access: it waits until the previous grid has completed
+// and its writes are visible, then lets the next kernel's CTAs be scheduled
+// as SMs free up (they too stop here until this grid has completed). Without
+// a programmatic predecessor the wait returns at once.
+__device__ __forceinline__ void grid_dependency_sync() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

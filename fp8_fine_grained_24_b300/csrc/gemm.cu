@@ -32,6 +32,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.h"
 #include "tmap.h"
 
 namespace fp8fg {
@@ -456,6 +457,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  grid_dependency_sync();
 
   if (warp < C::kEpiWarp0) {
    if constexpr (C::kRegSplit) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsLow));
@@ -833,7 +835,7 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
     return e;
   }
   if (!plan.sk) {
-    kernels[0]<<<plan.grid, C::kThreads, C::kSmem, stream>>>(tmA, tmB, tmSA, tmSB, tmC, a);
+    e = launch_kernel(kernels[0], dim3(plan.grid), dim3(C::kThreads), C::kSmem, stream, tmA, tmB, tmSA, tmSB, tmC, a);
   } else {
     a.dp_tiles = plan.dp_tiles;
     a.sk_tile0 = plan.dp_tiles;
@@ -842,9 +844,9 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
     a.sk_lcm = static_cast<int>(plan.sk_lcm);
     a.ws_partial = static_cast<float*>(p.workspace);
     a.ws_count = reinterpret_cast<int*>(static_cast<char*>(p.workspace) + plan.partial_bytes);
-    kernels[1]<<<plan.grid, C::kThreads, C::kSmem, stream>>>(tmA, tmB, tmSA, tmSB, tmC, a);
+    e = launch_kernel(kernels[1], dim3(plan.grid), dim3(C::kThreads), C::kSmem, stream, tmA, tmB, tmSA, tmSB, tmC, a);
   }
-  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) *detail = "GEMM kernel launch failed";
   return e;
 }

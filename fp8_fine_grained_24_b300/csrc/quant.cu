@@ -29,6 +29,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.h"
 #include "quant_math.cuh"
 #include "tmap.h"
 
@@ -177,6 +178,7 @@ __global__ void __launch_bounds__(32 * (1 + Op::kWarps), Op::kCtasPerSm)
     fence_barrier_init();
   }
   __syncthreads();
+  grid_dependency_sync();
 
   Walk w;
   Op::walk_init(a, w, blockIdx.x, gridDim.x);
@@ -717,8 +719,9 @@ cudaError_t launch_pipe(const CUtensorMap& tm, const CUtensorMap& tmo, const typ
   if (e != cudaSuccess) return e;
   const int64_t ctas = static_cast<int64_t>(num_sms) * Op::kCtasPerSm;
   const int64_t grid = a.chunks < ctas ? a.chunks : ctas;
-  quant_pipe_kernel<Op><<<static_cast<unsigned>(grid), 32 * (1 + Op::kWarps), Layout<Op>::kSmem, stream>>>(tm, tmo, a, p);
-  return cudaGetLastError();
+  e = launch_kernel(quant_pipe_kernel<Op>, dim3(static_cast<unsigned>(grid)), dim3(32 * (1 + Op::kWarps)),
+                    Layout<Op>::kSmem, stream, tm, tmo, a, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 CUtensorMapDataType map_type(int esz) {
