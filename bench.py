@@ -46,9 +46,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # reported traffic is null. Writes sit below M*N*2 because output lines still
 # in L2 when the kernel ends are written back after it.
 NCU_TRAFFIC = {
-    "kernel_sha": "b56ab55cb7560ed1",
-    "per_launch": {2112: 45535744 + 1134336, 24576: 210937088 + 179328512,
-                   7168: 82958848 + 36564224, 4096: 60056320 + 10929920},
+    "kernel_sha": "f4de3edff57967df",
+    "per_launch": {2112: 45521152 + 1225472, 24576: 210864128 + 179871744,
+                   7168: 82789376 + 36748288, 4096: 59965952 + 11442944},
 }
 
 
