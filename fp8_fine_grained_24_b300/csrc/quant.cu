@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(32 * (1 + Op::kWarps), Op::kCtasPerSm)
       mbar_init(bar0 + s * 8, 1);
       mbar_init(bar0 + (S + s) * 8, Op::kReleasers);
     }
-    for (int i = 0; i < Op::kExchBars; ++i) mbar_init(red_bar + i * 8, Op::kWarps);
+    for (int i = 0; i < Op::kExchBars; ++i) mbar_init(red_bar + i * 8, Op::kTeamWarps);
     fence_barrier_init();
   }
   __syncthreads();
@@ -351,23 +351,30 @@ struct Quant1x128 {
 
 // ------------------------------------------------------------ 128x128
 // Chunk: one 128x128 block (32 KB BF16 box; FP32 as two 64-row boxes),
-// k blocks fastest. Consumer warp w holds rows 8w .. 8w+7 in registers
-// (half-warp per row), reduces its amax, posts it to the exchange buffer and
-// arrives on the exchange barrier; after the barrier every warp has the
-// block's amax. The buffer is double-buffered by chunk parity: a warp can
-// only be one chunk ahead of the slowest, because the barrier needs all 16
-// arrivals.
+// k blocks fastest. The consumer warps of a team split the block's rows
+// (half-warp per row, 16 lanes x 8 elements), reduce their amax, post it to
+// the team's exchange buffer and arrive on the team's exchange barrier;
+// after the barrier every warp of the team has the block's amax. A team's
+// buffer is double-buffered by the parity of the team's chunks: a warp can
+// only be one chunk ahead of the slowest of its team, because the barrier
+// needs all of the team's arrivals.
+// BF16: two teams of 8 warps take alternate blocks, so that one team's
+// exchange wait overlaps the other's loads. A warp holds its 16 rows as raw
+// BF16 words (32 registers), takes the amax on packed pairs
+// (max.xorsign.abs.bf16x2 keeps |a| or |b|, the sign bit is dropped at the
+// end) and unpacks only for the quotient. FP32: one team of 16 warps of
+// 8 rows each.
 template <bool kF32>
 struct Quant128x128 {
   static constexpr int kEsz = kF32 ? 4 : 2;
   static constexpr int kStageBytes = kTile * kTile * kEsz;
   static constexpr int kBoxRows = kF32 ? 64 : 128;
-  static constexpr int kWarps = kConsumerWarps, kCtasPerSm = 1, kOutBytes = 0, kReleasers = kWarps;
-  static constexpr int kTeams = 1, kTeamWarps = kWarps;
+  static constexpr int kWarps = kConsumerWarps, kCtasPerSm = 1, kOutBytes = 0;
+  static constexpr int kTeams = kF32 ? 1 : 2, kTeamWarps = kWarps / kTeams, kReleasers = kTeamWarps;
   static constexpr int kStages = kRingBytes / kStageBytes;
-  static constexpr int kRedBytes = 2 * kConsumerWarps * 4;
-  static constexpr int kExchBars = 1;
-  static constexpr int kIters = kTile / kConsumerWarps / 2;
+  static constexpr int kRedBytes = kTeams * 2 * kTeamWarps * 4;
+  static constexpr int kExchBars = kTeams;
+  static constexpr int kIters = kTile / kTeamWarps / 2;  // row pairs per warp
   struct State {};
 
   struct Args {
@@ -394,42 +401,91 @@ struct Quant128x128 {
 
   static __device__ __forceinline__ void finish(const Args&, const Pipe&, int, int, State&) {}
 
+  // max(|x|) over a lane's packed BF16 words
+  static __device__ __forceinline__ float bf16_amax(const uint4 (&v)[kIters]) {
+    uint32_t m0 = 0, m1 = 0;
+#pragma unroll
+    for (int i = 0; i < kIters; ++i) {
+      asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m0) : "r"(v[i].x));
+      asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m1) : "r"(v[i].y));
+      asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m0) : "r"(v[i].z));
+      asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m1) : "r"(v[i].w));
+    }
+    asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m0) : "r"(m1));
+    return fmaxf(__uint_as_float((m0 << 16) & 0x7FFFFFFFu), __uint_as_float(m0 & 0x7FFF0000u));
+  }
+
   static __device__ __forceinline__ bool consume(const Args& a, const Pipe& p, const Walk& w, const Slot& sl,
                                                  int cw, int lane, State&) {
+    const int team = cw / kTeamWarps, wt = cw % kTeamWarps;
     const int half = lane >> 4, j = lane & 15;
+    const uint32_t tit = sl.it / kTeams;  // this team's chunk counter
     if (!wait_full(sl, p)) return false;
-    uint64_t v[kIters][4];
+    // FP32: a row's 8 elements are two 16-byte words; the lane keeps both
+    // halves of each row pair in consecutive entries
+    constexpr int kWords = kF32 ? 2 * kIters : kIters;
+    uint4 v[kWords];
 #pragma unroll
-    for (int i = 0; i < kIters; ++i)
-      load_neg8<kF32>(stage_of(sl) + ((cw * (2 * kIters) + 2 * i + half) * kTile + j * 8) * kEsz, v[i]);
-    float am = 0.0f;
+    for (int i = 0; i < kIters; ++i) {
+      const uint8_t* src = stage_of(sl) + ((wt * (2 * kIters) + 2 * i + half) * kTile + j * 8) * kEsz;
+      if constexpr (kF32) {
+        v[2 * i] = *reinterpret_cast<const uint4*>(src);
+        v[2 * i + 1] = *reinterpret_cast<const uint4*>(src + 16);
+      } else {
+        v[i] = *reinterpret_cast<const uint4*>(src);
+      }
+    }
+    float am;
+    if constexpr (kF32) {
+      am = 0.0f;
 #pragma unroll
-    for (int i = 0; i < kIters; ++i) am = fmaxf(am, amax4pk(v[i]));
+      for (int i = 0; i < kWords; ++i)
+        am = fmaxf(am, fmaxf(fmaxf(fabsf(__uint_as_float(v[i].x)), fabsf(__uint_as_float(v[i].y))),
+                             fmaxf(fabsf(__uint_as_float(v[i].z)), fabsf(__uint_as_float(v[i].w)))));
+    } else {
+      am = bf16_amax(v);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
     release(sl, lane);
-    float* rb = red_of(sl) + (sl.it & 1) * kConsumerWarps;
-    if (lane == 0) rb[cw] = am;
-    if (!exchange(sl, p, lane)) return false;
+    float* rb = red_of(sl) + (team * 2 + (tit & 1)) * kTeamWarps;
+    const uint32_t bar = sl.red_bar + team * 8;
+    if (lane == 0) rb[wt] = am;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+    if (!mbar_wait_sleep(bar, tit & 1, p.status, kStatusTimeoutQuantConsumer, p.wait_limit_ns)) return false;
     const float4* r4 = reinterpret_cast<const float4*>(rb);
 #pragma unroll
-    for (int i = 0; i < kConsumerWarps / 4; ++i) {
+    for (int i = 0; i < kTeamWarps / 4; ++i) {
       const float4 t = r4[i];
       am = fmaxf(am, fmaxf(fmaxf(t.x, t.y), fmaxf(t.z, t.w)));
     }
     const float sc = tile_scale(am, a.pow2 != 0);
     const float rc = __frcp_rn(sc);
     const int path = make_tile_div_mode(sc);  // the same block scale in every lane
-    const int row_in = w.d1 * kTile + cw * (2 * kIters) + half;
+    const int row_in = w.d1 * kTile + wt * (2 * kIters) + half;
     uint8_t* qp = a.q + (w.d2 * a.N + row_in) * a.K + static_cast<int64_t>(w.d0) * kTile + j * 8;
     const int64_t rows_left = a.N - row_in;
 #pragma unroll
     for (int i = 0; i < kIters; ++i) {
-      quot2_n<4>(v[i], path, sc, rc);
-      if (2 * i < rows_left) *reinterpret_cast<uint2*>(qp) = codes8(v[i]);
+      uint64_t x[4];
+      if constexpr (kF32) {
+        const uint4 lo = v[2 * i], hi = v[2 * i + 1];
+        x[0] = pk2(-__uint_as_float(lo.x), -__uint_as_float(lo.y));
+        x[1] = pk2(-__uint_as_float(lo.z), -__uint_as_float(lo.w));
+        x[2] = pk2(-__uint_as_float(hi.x), -__uint_as_float(hi.y));
+        x[3] = pk2(-__uint_as_float(hi.z), -__uint_as_float(hi.w));
+      } else {
+        x[0] = neg_bf16x2(v[i].x);
+        x[1] = neg_bf16x2(v[i].y);
+        x[2] = neg_bf16x2(v[i].z);
+        x[3] = neg_bf16x2(v[i].w);
+      }
+      quot2_n<4>(x, path, sc, rc);
+      if (2 * i < rows_left) *reinterpret_cast<uint2*>(qp) = codes8(x);
       qp += 2 * a.K;
     }
-    if (cw == 0 && lane == 0) a.s[(w.d2 * a.NB + w.d1) * a.KB + w.d0] = sc;
+    if (wt == 0 && lane == 0) a.s[(w.d2 * a.NB + w.d1) * a.KB + w.d0] = sc;
     return true;
   }
 };
