@@ -83,33 +83,7 @@ struct Walk {
   }
 };
 
-// Eight consecutive elements of a row from shared memory, negated, as four
-// f32 pairs.
-template <bool kF32>
-__device__ __forceinline__ void load_neg8(const uint8_t* p, uint64_t (&v)[4]) {
-  if constexpr (kF32) {
-    const float4 a = *reinterpret_cast<const float4*>(p);
-    const float4 b = *reinterpret_cast<const float4*>(p + 16);
-    v[0] = pk2(-a.x, -a.y);
-    v[1] = pk2(-a.z, -a.w);
-    v[2] = pk2(-b.x, -b.y);
-    v[3] = pk2(-b.z, -b.w);
-  } else {
-    const uint4 w = *reinterpret_cast<const uint4*>(p);
-    v[0] = neg_bf16x2(w.x);
-    v[1] = neg_bf16x2(w.y);
-    v[2] = neg_bf16x2(w.z);
-    v[3] = neg_bf16x2(w.w);
-  }
-}
-
-__device__ __forceinline__ float amax4pk(const uint64_t (&v)[4]) {
-  float a = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) a = amax_pk(v[i], a);
-  return a;
-}
-
+// Eight quotients (four pairs) -> eight E4M3 bytes, the first in the low byte.
 __device__ __forceinline__ uint2 codes8(const uint64_t (&v)[4]) {
   return make_uint2(e4m3x4_pk(v[0], v[1]), e4m3x4_pk(v[2], v[3]));
 }
@@ -252,36 +226,34 @@ __device__ __forceinline__ void release(const Slot& sl, int lane) {
   if (lane == 0) mbar_arrive(sl.empty);
 }
 
-// Post this warp's partial maxima (written before the call) and wait until
-// all 16 consumer warps have posted theirs for this chunk.
-__device__ __forceinline__ bool exchange(const Slot& sl, const Pipe& p, int lane) {
-  __syncwarp();
-  if (lane == 0) mbar_arrive(sl.red_bar);
-  return mbar_wait_sleep(sl.red_bar, sl.it & 1, p.status, kStatusTimeoutQuantConsumer, p.wait_limit_ns);
-}
-
 // ------------------------------------------------------------ 1x128
 // Chunk: rows [rb*R, rb*R + R) x columns [kb*128, kb*128 + 128), R = 128
-// (BF16) or 64 (FP32), one 32 KB TMA box; kb runs fastest. Consumer warp w
-// takes 2*I rows (I = R/32); each half-warp one row per step (16 lanes x 8
-// elements), so a warp reads 2 rows per shared-memory instruction and writes
-// two 128-byte row segments of q. The scalar work of a tile (the division
-// by 448, the reciprocal) is done once per tile rather than on each of its
-// 16 lanes: the warp's 2*I row maxima are gathered one per lane, every lane
-// computes one scale, and each step fetches its tile's scale by shuffle.
+// (BF16) or 64 (FP32), one 32 KB TMA box; kb runs fastest. A warp takes
+// 2*I consecutive rows of the chunk; each half-warp one row per step (16
+// lanes x 8 elements), so a warp reads 2 rows per shared-memory instruction
+// and writes two 128-byte row segments of q. The scalar work of a tile (the
+// division by 448, the reciprocal) is done once per tile rather than on each
+// of its 16 lanes: the warp's 2*I row maxima are gathered one per lane,
+// every lane computes one scale, and each step fetches its tile's scale by
+// shuffle.
+// BF16: two teams of 8 warps take alternate chunks (I = 8), so that the
+// shuffle and scale chains of one chunk overlap another's; a lane keeps
+// its rows as raw BF16 words, takes the row maxima on packed pairs and
+// unpacks only for the quotient. FP32: one team of 16 warps (I = 2).
 template <bool kF32>
 struct Quant1x128 {
   static constexpr int kEsz = kF32 ? 4 : 2;
   static constexpr int kRows = kF32 ? 64 : 128;
   static constexpr int kStageBytes = kRows * kTile * kEsz;
-  static constexpr int kWarps = kConsumerWarps, kCtasPerSm = 1, kOutBytes = 0, kReleasers = kWarps;
-  static constexpr int kTeams = 1, kTeamWarps = kWarps;
+  static constexpr int kWarps = kConsumerWarps, kCtasPerSm = 1, kOutBytes = 0;
+  static constexpr int kTeams = kF32 ? 1 : 2, kTeamWarps = kWarps / kTeams, kReleasers = kTeamWarps;
   static constexpr int kStages = kRingBytes / kStageBytes;
   static constexpr int kRedBytes = 0;
   static constexpr int kExchBars = 0;
-  static constexpr int kIters = kRows / kConsumerWarps / 2;  // 4 (BF16) or 2 (FP32)
-  struct State {};
+  static constexpr int kIters = kRows / kTeamWarps / 2;  // 8 (BF16) or 2 (FP32)
   static constexpr int kWarpRows = 2 * kIters;
+  static_assert(kWarpRows <= 32, "one row maximum per lane");
+  struct State {};
 
   struct Args {
     int64_t chunks, M, K, lds;
@@ -306,17 +278,37 @@ struct Quant1x128 {
 
   static __device__ __forceinline__ bool consume(const Args& a, const Pipe& p, const Walk& w, const Slot& sl,
                                                  int cw, int lane, State&) {
+    const int wt = cw % kTeamWarps;
     const int half = lane >> 4, j = lane & 15;
     if (!wait_full(sl, p)) return false;
-    uint64_t v[kIters][4];
+    // the lane's 8 elements of row 2i + half, raw (BF16: one 16-byte word;
+    // FP32: two)
+    constexpr int kWords = kF32 ? 2 : 1;
+    uint4 v[kIters][kWords];
 #pragma unroll
-    for (int i = 0; i < kIters; ++i)
-      load_neg8<kF32>(stage_of(sl) + ((cw * kWarpRows + 2 * i + half) * kTile + j * 8) * kEsz, v[i]);
+    for (int i = 0; i < kIters; ++i) {
+      const uint8_t* src = stage_of(sl) + ((wt * kWarpRows + 2 * i + half) * kTile + j * 8) * kEsz;
+#pragma unroll
+      for (int u = 0; u < kWords; ++u) v[i][u] = *reinterpret_cast<const uint4*>(src + 16 * u);
+    }
     // row maxima: after the xor-shuffles every lane of half h holds am[i] of row 2i+h
     float am[kIters];
 #pragma unroll
     for (int i = 0; i < kIters; ++i) {
-      am[i] = amax4pk(v[i]);
+      if constexpr (kF32) {
+        float m = 0.0f;
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+          m = fmaxf(m, fmaxf(fmaxf(fabsf(__uint_as_float(v[i][u].x)), fabsf(__uint_as_float(v[i][u].y))),
+                             fmaxf(fabsf(__uint_as_float(v[i][u].z)), fabsf(__uint_as_float(v[i][u].w)))));
+        am[i] = m;
+      } else {
+        uint32_t m0 = v[i][0].x, m1 = v[i][0].z;
+        asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m0) : "r"(v[i][0].y));
+        asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m1) : "r"(v[i][0].w));
+        asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m0) : "r"(m1));
+        am[i] = fmaxf(__uint_as_float((m0 << 16) & 0x7FFFFFFFu), __uint_as_float(m0 & 0x7FFF0000u));
+      }
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) am[i] = fmaxf(am[i], __shfl_xor_sync(0xffffffffu, am[i], o));
     }
@@ -332,7 +324,7 @@ struct Quant1x128 {
     const float my_s = tile_scale(my_am, a.pow2 != 0);
     const float my_r = __frcp_rn(my_s);
     const int path = warp_quot_mode(make_tile_div_mode(my_s));
-    const int64_t row0 = w.d2 * kRows + cw * kWarpRows;
+    const int64_t row0 = w.d2 * kRows + wt * kWarpRows;
     const int64_t col = static_cast<int64_t>(w.d0) * kTile;
     if (lane < kWarpRows && row0 + lane < a.M) a.s[w.d0 * a.lds + row0 + lane] = my_s;
     uint8_t* qp = a.q + (row0 + half) * a.K + col + j * 8;
@@ -341,8 +333,20 @@ struct Quant1x128 {
     for (int i = 0; i < kIters; ++i) {
       const float sc = __shfl_sync(0xffffffffu, my_s, 2 * i + half);
       const float rc = __shfl_sync(0xffffffffu, my_r, 2 * i + half);
-      quot2_n<4>(v[i], path, sc, rc);
-      if (2 * i < rows_left) *reinterpret_cast<uint2*>(qp) = codes8(v[i]);
+      uint64_t x[4];
+      if constexpr (kF32) {
+        x[0] = pk2(-__uint_as_float(v[i][0].x), -__uint_as_float(v[i][0].y));
+        x[1] = pk2(-__uint_as_float(v[i][0].z), -__uint_as_float(v[i][0].w));
+        x[2] = pk2(-__uint_as_float(v[i][1].x), -__uint_as_float(v[i][1].y));
+        x[3] = pk2(-__uint_as_float(v[i][1].z), -__uint_as_float(v[i][1].w));
+      } else {
+        x[0] = neg_bf16x2(v[i][0].x);
+        x[1] = neg_bf16x2(v[i][0].y);
+        x[2] = neg_bf16x2(v[i][0].z);
+        x[3] = neg_bf16x2(v[i][0].w);
+      }
+      quot2_n<4>(x, path, sc, rc);
+      if (2 * i < rows_left) *reinterpret_cast<uint2*>(qp) = codes8(x);
       qp += 2 * a.K;
     }
     return true;
