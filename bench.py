@@ -46,9 +46,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # reported traffic is null. Writes sit below M*N*2 because output lines still
 # in L2 when the kernel ends are written back after it.
 NCU_TRAFFIC = {
-    "kernel_sha": "f4de3edff57967df",
-    "per_launch": {2112: 45521152 + 1225472, 24576: 210864128 + 179871744,
-                   7168: 82789376 + 36748288, 4096: 59965952 + 11442944},
+    "kernel_sha": "a4090ab6045dec23",
+    "per_launch": {2112: 45526528 + 1128704, 24576: 210935296 + 179408128,
+                   7168: 82904320 + 36682240, 4096: 59996416 + 11173632},
 }
 
 
