@@ -183,9 +183,38 @@ __device__ __forceinline__ Tile decode_tile(const KArgs& a, int t) {
   return ti;
 }
 
+// Masked rows: the active M blocks of group g, its first
+// ceil(masked[g] / BM) (at most tiles_m).
+__device__ __forceinline__ int masked_mblocks(const KArgs& a, int g) {
+  int mk = __ldg(a.masked + g);
+  mk = mk < 0 ? 0 : mk;
+  const int mb = (mk + BM - 1) / BM;
+  return mb < a.tiles_m ? mb : a.tiles_m;
+}
+
+// Masked rows: active tile j in group order, M blocks fastest inside a
+// group, so that a group's M blocks read each B tile at about the same time.
+// False when there are at most j active tiles.
+template <int BN>
+__device__ __forceinline__ bool decode_masked_tile(const KArgs& a, int j, Tile& ti) {
+  const int groups = a.num_tiles / (a.tiles_m * a.tiles_n);
+  for (int g = 0; g < groups; ++g) {
+    const int mbs = masked_mblocks(a, g);
+    if (j < mbs * a.tiles_n) {
+      const int nb = j / mbs;
+      ti = decode_tile<BN>(a, (g * a.tiles_n + nb) * a.tiles_m + (j - nb * mbs));
+      return true;
+    }
+    j -= mbs * a.tiles_n;
+  }
+  return false;
+}
+
 // This CTA's work in order: whole tiles t = blockIdx.x + i * gridDim.x below
-// dp_tiles (all tiles without Stream-K), then its Stream-K unit range cut at
-// tile boundaries into segments.
+// dp_tiles (all tiles without Stream-K; for masked rows, the active tiles
+// only, found from the device-side row counts, so that every CTA gets an
+// equal share of real work), then its Stream-K unit range cut at tile
+// boundaries into segments.
 struct Work {
   int t, u, end;
 };
@@ -195,6 +224,7 @@ __device__ __forceinline__ Work work_begin(const KArgs& a) {
   Work w;
   w.t = blockIdx.x;
   w.u = w.end = 0;
+
   if constexpr (kSK) {
     const int64_t u = static_cast<int64_t>(blockIdx.x) * a.sk_per_cta;
     const int64_t e = u + a.sk_per_cta;
@@ -204,9 +234,15 @@ __device__ __forceinline__ Work work_begin(const KArgs& a) {
   return w;
 }
 
-template <int BN, bool kSK>
+// kCompact (masked rows only): the tiles are the active ones.
+template <int BN, bool kSK, bool kCompact>
 __device__ __forceinline__ bool work_next(const KArgs& a, Work& w, Tile& ti) {
   const int dp = kSK ? a.dp_tiles : a.num_tiles;
+  if constexpr (kCompact) {
+    if (!decode_masked_tile<BN>(a, w.t, ti)) return false;
+    w.t += gridDim.x;
+    return true;
+  }
   if (w.t < dp) {
     ti = decode_tile<BN>(a, w.t);
     w.t += gridDim.x;
@@ -408,7 +444,7 @@ __device__ __forceinline__ void promote(float* acc, const uint32_t (&r)[W], floa
   }
 }
 
-template <int BN, bool kBRow, bool kF32, bool kSplit>
+template <int BN, bool kBRow, bool kF32, bool kSplit, bool kCompact>
 __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
@@ -469,7 +505,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       bool ok = true;
       Work wk = work_begin<kSplit>(a);
       Tile ti;
-      while (ok && work_next<BN, kSplit>(a, wk, ti)) {
+      while (ok && work_next<BN, kSplit, kCompact>(a, wk, ti)) {
         if (ti.skip) continue;
         for (int kb = ti.kb0; kb < ti.kb0 + ti.kbc; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1;
@@ -501,7 +537,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       bool ok = true;
       Work wk = work_begin<kSplit>(a);
       Tile ti;
-      while (ok && work_next<BN, kSplit>(a, wk, ti)) {
+      while (ok && work_next<BN, kSplit, kCompact>(a, wk, ti)) {
         if (ti.skip) continue;
         for (int kb = ti.kb0; kb < ti.kb0 + ti.kbc; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1;
@@ -551,7 +587,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     int held = -1;  // pipeline stage kept for staging (kStage, warps < kBorrowWarps)
     Work wk = work_begin<kSplit>(a);
     Tile ti;
-    while (ok && work_next<BN, kSplit>(a, wk, ti)) {
+    while (ok && work_next<BN, kSplit, kCompact>(a, wk, ti)) {
       if (ti.skip) continue;
 #pragma unroll
       for (int j = 0; j < NC; ++j) acc[j] = 0.0f;
@@ -661,7 +697,7 @@ int64_t ld4(int64_t r) { return (r + 3) / 4 * 4; }
 
 // Raise the kernel's dynamic shared-memory limit once per device (the call
 // costs tens of microseconds of host time, so it is not repeated per launch).
-template <int BN, bool kBRow, bool kF32, bool kSplit>
+template <int BN, bool kBRow, bool kF32, bool kSplit, bool kCompact>
 cudaError_t ensure_smem_attr() {
   static std::atomic<uint64_t> done{0};
   int dev = 0;
@@ -675,12 +711,12 @@ cudaError_t ensure_smem_attr() {
     // raised counts, forever if it never can: refuse to launch a build whose
     // register count does not cover the split.
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, fp8_gemm_kernel<BN, kBRow, kF32, kSplit>);
+    e = cudaFuncGetAttributes(&fa, fp8_gemm_kernel<BN, kBRow, kF32, kSplit, kCompact>);
     if (e != cudaSuccess) return e;
     if (static_cast<long>(fa.numRegs) * C::kThreads < 128L * C::kRegsLow + 256L * C::kRegsHigh)
       return cudaErrorInvalidConfiguration;
   }
-  e = cudaFuncSetAttribute(fp8_gemm_kernel<BN, kBRow, kF32, kSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(fp8_gemm_kernel<BN, kBRow, kF32, kSplit, kCompact>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg<BN>::kSmem);
   if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
   return e;
@@ -813,16 +849,20 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
                               p.workspace != nullptr ? p.workspace_bytes : 0);
 
   using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, KArgs);
-  KernelFn kernels[2] = {nullptr, nullptr};  // without / with Stream-K
+  // whole tiles / Stream-K / active tiles of the masked-rows layout
+  KernelFn kernels[3] = {nullptr, nullptr, nullptr};
+  const bool masked = p.mode == kModeMaskedRows;
   cudaError_t e = cudaSuccess;
   const int variant = (p.b_row ? 4 : 0) + (p.out_f32 ? 2 : 0);
   switch (variant) {
 #define FP8FG_VARIANT(V, R, F)                                                   \
   case V:                                                                        \
-    kernels[0] = fp8_gemm_kernel<BN, R, F, false>;                               \
-    kernels[1] = fp8_gemm_kernel<BN, R, F, true>;                                \
-    e = ensure_smem_attr<BN, R, F, false>();                                     \
-    if (e == cudaSuccess && plan.sk) e = ensure_smem_attr<BN, R, F, true>();     \
+    kernels[0] = fp8_gemm_kernel<BN, R, F, false, false>;                        \
+    kernels[1] = fp8_gemm_kernel<BN, R, F, true, false>;                         \
+    kernels[2] = fp8_gemm_kernel<BN, R, F, false, true>;                         \
+    e = masked ? ensure_smem_attr<BN, R, F, false, true>()                       \
+               : ensure_smem_attr<BN, R, F, false, false>();                     \
+    if (e == cudaSuccess && plan.sk) e = ensure_smem_attr<BN, R, F, true, false>(); \
     break;
     FP8FG_VARIANT(0, false, false)
     FP8FG_VARIANT(2, false, true)
@@ -835,7 +875,7 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
     return e;
   }
   if (!plan.sk) {
-    e = launch_kernel(kernels[0], dim3(plan.grid), dim3(C::kThreads), C::kSmem, stream, tmA, tmB, tmSA, tmSB, tmC, a);
+    e = launch_kernel(kernels[masked ? 2 : 0], dim3(plan.grid), dim3(C::kThreads), C::kSmem, stream, tmA, tmB, tmSA, tmSB, tmC, a);
   } else {
     a.dp_tiles = plan.dp_tiles;
     a.sk_tile0 = plan.dp_tiles;
