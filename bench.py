@@ -46,9 +46,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # reported traffic is null. Writes sit below M*N*2 because output lines still
 # in L2 when the kernel ends are written back after it.
 NCU_TRAFFIC = {
-    "kernel_sha": "a4090ab6045dec23",
-    "per_launch": {2112: 45526528 + 1128704, 24576: 210935296 + 179408128,
-                   7168: 82904320 + 36682240, 4096: 59996416 + 11173632},
+    "kernel_sha": "cb0c247e1a6de545",
+    "per_launch": {2112: 45523200 + 1278208, 24576: 210401280 + 180621568,
+                   7168: 83070464 + 37059072, 4096: 60042752 + 11343872},
 }
 
 
