@@ -73,14 +73,6 @@ __device__ __forceinline__ int make_tile_div_mode(float s) {
   return s < 0x1p-80f ? kQuotDiv : kQuotFma;
 }
 
-__device__ __forceinline__ TileDiv make_tile_div(float s) {
-  TileDiv d;
-  d.s = s;
-  d.r = __frcp_rn(s);
-  d.mode = make_tile_div_mode(s);
-  return d;
-}
-
 __device__ __forceinline__ float quot_fma(float x, float s, float r) {
   float q = __fmul_rn(x, r);
   float e = __fmaf_rn(s, q, -x);
@@ -95,21 +87,6 @@ __device__ __forceinline__ float tile_quot(float x, const TileDiv& d) {
   return quot_fma(x, d.s, d.r);
 }
 
-// Quotients of N elements with the mode test hoisted out of the loop.
-template <int N>
-__device__ __forceinline__ void tile_quot_n(float (&v)[N], const TileDiv& d) {
-  if (d.mode == kQuotMul) {
-#pragma unroll
-    for (int i = 0; i < N; ++i) v[i] = __fmul_rn(v[i], d.r);
-  } else if (d.mode == kQuotFma) {
-#pragma unroll
-    for (int i = 0; i < N; ++i) v[i] = quot_fma(v[i], d.s, d.r);
-  } else {
-#pragma unroll
-    for (int i = 0; i < N; ++i) v[i] = __fdiv_rn(v[i], d.s);
-  }
-}
-
 // The quotient path for a set of tiles whose scales lanes hold: kQuotMul if
 // every scale is a normal power of two, else kQuotFma if every scale allows
 // it, else kQuotDiv (per-element tile_quot). Uniform across the warp.
@@ -117,27 +94,6 @@ __device__ __forceinline__ int warp_quot_mode(int my_mode) {
   if (__all_sync(0xffffffffu, my_mode == kQuotMul)) return kQuotMul;
   if (__all_sync(0xffffffffu, my_mode != kQuotDiv)) return kQuotFma;
   return kQuotDiv;
-}
-
-// Quotients of N elements by (s, r) along a path chosen by warp_quot_mode.
-// kQuotFma is exact for any scale that is not kQuotDiv (a power of two
-// included); kQuotDiv falls back to the per-tile choice.
-template <int N>
-__device__ __forceinline__ void quot_n(float (&v)[N], int path, float s, float r) {
-  if (path == kQuotMul) {
-#pragma unroll
-    for (int i = 0; i < N; ++i) v[i] = __fmul_rn(v[i], r);
-  } else if (path == kQuotFma) {
-#pragma unroll
-    for (int i = 0; i < N; ++i) v[i] = quot_fma(v[i], s, r);
-  } else {
-    TileDiv d;
-    d.s = s;
-    d.r = r;
-    d.mode = make_tile_div_mode(s);
-#pragma unroll
-    for (int i = 0; i < N; ++i) v[i] = tile_quot(v[i], d);
-  }
 }
 
 // ---------------------------------------------------------------- packed
@@ -169,29 +125,9 @@ __device__ __forceinline__ uint32_t e4m3x4_pk(uint64_t q01, uint64_t q23) {
   return d;
 }
 
-// Pairs (c0, c1) of quotients of four consecutive tokens -> the E4M3 codes
-// of channel c0 for the four tokens in `lo` and of channel c1 in `hi`
-// (first token in the low byte): two bytes per conversion, then a byte
-// transpose by permutes.
-__device__ __forceinline__ void e4m3_transpose4(uint64_t q0, uint64_t q1, uint64_t q2, uint64_t q3, uint32_t& lo,
-                                                uint32_t& hi) {
-  asm("{\n\t.reg .f32 a0, a1, a2, a3, a4, a5, a6, a7;\n\t.reg .b16 h0, h1, h2, h3;\n\t"
-      ".reg .b32 w01, w23;\n\t"
-      "mov.b64 {a0, a1}, %2;\n\tmov.b64 {a2, a3}, %3;\n\t"
-      "mov.b64 {a4, a5}, %4;\n\tmov.b64 {a6, a7}, %5;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 h0, a1, a0;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 h1, a3, a2;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 h2, a5, a4;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 h3, a7, a6;\n\t"
-      "mov.b32 w01, {h0, h1};\n\tmov.b32 w23, {h2, h3};\n\t"
-      "prmt.b32 %0, w01, w23, 0x6420;\n\t"
-      "prmt.b32 %1, w01, w23, 0x7531;\n\t}"
-      : "=r"(lo), "=r"(hi)
-      : "l"(q0), "l"(q1), "l"(q2), "l"(q3));
-}
-
 // N pairs of negated values -> quotients along a path chosen by
-// warp_quot_mode (see quot_n).
+// warp_quot_mode: kQuotFma is exact for any scale that is not kQuotDiv (a
+// power of two included); kQuotDiv falls back to the per-tile choice.
 template <int N>
 __device__ __forceinline__ void quot2_n(uint64_t (&v)[N], int path, float s, float r) {
   if (path == kQuotMul) {
@@ -219,32 +155,6 @@ __device__ __forceinline__ void quot2_n(uint64_t (&v)[N], int path, float s, flo
 // -lo = (w << 16) + 2^31 (mod 2^32) flips the sign bit, -hi likewise.
 __device__ __forceinline__ uint64_t neg_bf16x2(uint32_t w) {
   return pk2(__uint_as_float(w * 65536u + 0x80000000u), __uint_as_float((w & 0xFFFF0000u) ^ 0x80000000u));
-}
-
-__device__ __forceinline__ float amax_pk(uint64_t v, float a) {
-  const float2 f = unpk2(v);
-  return fmaxf(a, fmaxf(fabsf(f.x), fabsf(f.y)));
-}
-
-// Two floats -> two E4M3 bytes (RNE, satfinite); x in the low byte.
-__device__ __forceinline__ uint32_t e4m3x2(float x, float y) {
-  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(x, y), __NV_SATFINITE, __NV_E4M3));
-}
-
-// Four floats -> four E4M3 bytes, v[0] in the low byte.
-__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
-  return e4m3x2(a, b) | (e4m3x2(c, d) << 16);
-}
-
-__device__ __forceinline__ float e4m3_to_f32(uint8_t v) {
-  __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(v), __NV_E4M3);
-  return __half2float(__half(h));
-}
-
-// The two E4M3 bytes in the low 16 bits of w -> two floats (exact).
-__device__ __forceinline__ float2 e4m3x2_to_f32(uint32_t w) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xFFFFu), __NV_E4M3);
-  return __half22float2(*reinterpret_cast<__half2*>(&h));
 }
 
 // Four floats -> four E4M3 bytes (RNE, satfinite), a in the low byte.
@@ -279,8 +189,5 @@ __device__ __forceinline__ uint64_t e4m3x2_hi_pk(uint32_t w) {
       : "r"(w));
   return r;
 }
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 }  // namespace fp8fg
