@@ -205,6 +205,14 @@ def test_masked_small(lib):
     _masked_case(lib, 4, 256, 264, 384, np.array([0, 256, 17, 129], np.int32), 51)
 
 
+def test_masked_sparse_experts(lib):
+    # the active tiles are enumerated on the device across all experts: most
+    # experts empty, one row, a partial and a full expert, the last one last
+    masked = np.zeros(40, np.int32)
+    masked[3], masked[17], masked[39] = 1, 200, 256
+    _masked_case(lib, 40, 256, 264, 256, masked, 57)
+
+
 def test_masked_decode_like(lib):
     masked = wl.masked_counts(6, 256, seed=52)
     _masked_case(lib, 6, 256, 512, 1024, masked, 53)
