@@ -26,7 +26,7 @@
 //     ordering) race on it and may produce wrong results: order them.
 //   * A problem whose scratch need exceeds the array is rejected with
 //     FP8FG_ERR_UNSUPPORTED_SHAPE before anything is enqueued.
-//   * The part of the scratch that must start at zero (the split-K arrival
+//   * The part of the scratch that must start at zero (the Stream-K arrival
 //     counters) is cleared on the caller's stream by every call.
 #include <mutex>
 

@@ -145,8 +145,8 @@ FP8FG_API int fp8_requant_128x1(const void* src, int src_dtype, const float* s_s
  *   accumulate 1: C += result (FP32 output only: weight-gradient
  *              accumulation); 0: C = result
  *   workspace  device scratch for splitting tiles along K over several SMs
- *              (Stream-K): when M is too small to occupy the GPU (decode),
- *              and when the last wave of output tiles would leave SMs idle.
+ *              (Stream-K), used when the output has too few tiles to occupy
+ *              the GPU (at most half as many as SMs: decode-sized M).
  *              fp8fg_gemm_workspace_size(M, N, K) bytes, 16-byte aligned,
  *              zero-filled before its first use; every call leaves its
  *              counters zero-filled again (re-zero the workspace after a call
