@@ -6,14 +6,17 @@
 //                 transposed (channel-major).
 //
 // All three are the same persistent pipeline. One CTA per SM; warp 0 is a
-// TMA producer that streams the input in 16-64 KB chunks (one 128-column
-// strip of rows, one 128x128 block, one 128x128 tile) through a ring of
-// shared-memory stages; 16 consumer warps read a chunk from shared memory
-// into registers, release the stage, reduce the amax (warp shuffles, and for
-// the 2-D tiles partial maxima exchanged through shared memory behind an
-// mbarrier), then write E4M3 codes and scales straight to global memory
-// with row-contiguous stores. The ring keeps about 192 KB of loads in
-// flight per SM, so HBM streams continuously while the consumers compute.
+// TMA producer that streams the input in 16-64 KB chunks (128 rows x 128
+// columns of activations, one 128x128 weight block, one 128-token x
+// 128-channel tile) through a ring of shared-memory stages. 16 consumer
+// warps, in two teams of 8 that take alternate chunks (one team of 16 for
+// FP32 activations and weights), read a chunk into registers, release the
+// stage and reduce the amax: warp shuffles, and for 128x128 blocks per-warp
+// maxima exchanged through shared memory behind an mbarrier. They write the
+// E4M3 codes and scales with row-contiguous global stores; the transposed
+// 128x1 output goes through a swizzled image in shared memory and one TMA
+// store per warp. The ring keeps about 200 KB of loads in flight per SM, so
+// HBM streams continuously while the consumers compute.
 //
 // The consumers are bound by instruction issue, so the element arithmetic
 // is kept lean: values are unpacked already negated (free for BF16) so that
@@ -50,7 +53,8 @@ struct Pipe {
 };
 
 // Chunk coordinates (d2, d1, d0) of chunk index c = (d2 * R1 + d1) * R0 + d0,
-// advanced by a fixed step (gridDim.x) with carries instead of divisions.
+// advanced by a fixed step (the CTAs, times the teams) with carries instead
+// of divisions.
 struct Walk {
   int64_t d2;
   int d1, d0;
