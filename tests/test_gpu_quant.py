@@ -194,7 +194,7 @@ def test_quant_128x128_ring_wrap(lib):
 @pytest.mark.slow
 @pytest.mark.parametrize("pow2", [False, True])
 def test_requant_ring_wrap(lib, pow2):
-    T, C = 4096, 8192  # E4M3 source: 32 x 64 tiles, 12 stages
+    T, C = 4096, 8192  # E4M3 source: 32 x 64 tiles, 11 stages
     x = wl.activations(T, C, seed=6, device="cpu", dtype=torch.float32).numpy()
     q, s = quant.quant_1x128(x)
     s_pad = np.zeros((C // 128, ld4(T)), np.float32)
