@@ -197,6 +197,22 @@ class PrefillStep:
                                                             workspace=self.ws))
 
 
+# ---------------------------------------------------------------- replicas
+def slowest_replica_ms(total_ms, dist, device):
+    """The job's timed span: the maximum over ranks of each replica's span
+    (every rank must call this; without a process group it is the local span)."""
+    import torch
+    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_step, world, ms_per_step):
+    """Whole-job rate: the units all `world` replicas processed per second."""
+    return units_per_step * world / (ms_per_step * 1e-3)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import fp8_fine_grained_24_b300 as fg
@@ -238,10 +254,7 @@ def run_ours(args, rank, world, local_rank):
     per_kind = {}
     for kind, s, e in events:
         per_kind.setdefault(kind, []).append(s.elapsed_time(e))
-    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = slowest_replica_ms(total_ms, dist, device)
     ms_per_step = total_ms / args.steps
 
     # ---- end to end through the public API with host buffers
@@ -266,7 +279,7 @@ def run_ours(args, rank, world, local_rank):
     if NCU_TRAFFIC["kernel_sha"] == sha:
         # mean over the step's four launches, like `achieved`
         traffic = round(statistics.mean(NCU_TRAFFIC["per_launch"][n] for n in N_PREFILL))
-    value = step.flops * world / (ms_per_step * 1e-3) / 1e12
+    value = job_throughput(step.flops, world, ms_per_step) / 1e12
     line = {
         "metric": METRIC,
         "value": round(value, 2),
