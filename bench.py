@@ -232,11 +232,11 @@ def run_ours(args, rank, world, local_rank):
     step = PrefillStep(fg, torch, device)
     clocks = ClockSampler(local_rank)
     clocks.start()
+    time.sleep(0.3)  # let the sampler start (before the warm-up: no idle gap before the timed steps)
     for _ in range(args.warmup):
         step.run()
     fg.check()
     barrier()
-    time.sleep(0.3)  # let the sampler start
 
     events = []
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
