@@ -7,7 +7,8 @@ to E5M2) and the OCP 8-bit floating point specification defines it (the
 the largest finite magnitude is 1.75 * 2^8 = 448. Exponent 0000 encodes
 subnormals m * 2^-9.
 
-Encoding used by the quantizers (reading fixed for this build): round to
+Encoding used by the quantizers (the pages name E4M3 but not its rounding;
+this is the reading taken): round to
 nearest on the exact value with ties to the even code, and saturate every
 finite magnitude that would land above 448 to 448 (the ``satfinite`` mode).
 The sign bit is copied from the input, so values that round to zero keep

@@ -4,7 +4,7 @@ Inputs come from the seeded generators in ``workloads``; expected values come
 from ``oracle`` only (never from the CUDA path). Scale arrays are moved
 between the oracle's logical layout and the library's padded row stride.
 
-GEMM tolerance (stated for this build; see the design notes): against the
+GEMM tolerance: against the
 oracle's FP64 product Cref of the same dequantized operands,
   * relative Frobenius error <= 1e-3, measured against Cref rounded to the
     output type (BF16 output is compared with the oracle's own RNE rounding
