@@ -10,7 +10,16 @@ Printed metric: FP8 GEMM TFLOP/s of the whole step (2*M*N*K summed over the
 four weights, divided by the step time), with the GEMM kernel's roofline
 fraction (against the FP8 tensor peak) and the quantizers' HBM fraction.
 
-Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--all]
+Timing: the K timed steps are captured once into a CUDA graph, with a timing
+event node around every kernel, and the graph is replayed inside the timed
+region (host launch overhead stays out of the device time; an eager reading
+of the same steps is reported beside it). Warm-up runs W eager steps and at
+least a second of work. The line's ``configs`` object adds one graph-timed
+entry per other workload (decode, grouped MoE, masked MoE, weight gradient,
+requantization, small dense case) with its roofline fraction.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+       python bench.py --case CASE --shape ...   (one kernel, see run_case)
 With N>1 (torchrun), every rank runs the same workload on its own GPU
 (independent replicas: the path has no exchange step); rank 0 prints.
 """
@@ -158,6 +167,8 @@ class ClockSampler:
 class PrefillStep:
     """Device-resident buffers and the launches of one step."""
 
+    KINDS = ("quant_1x128", "quant_128x128", "gemm")
+
     def __init__(self, fg, torch, device, seed=1001):
         import workloads as wl
         self.fg, self.torch = fg, torch
@@ -177,14 +188,18 @@ class PrefillStep:
         self.launches = 1 + 2 * len(N_PREFILL)
 
     def run(self, events=None):
-        """Enqueue one step; if `events` is a list, append (kind, start, end) event pairs."""
+        """Enqueue one step on the current stream. If `events` is a list,
+        bracket every launch with a pair of timing events (appended as
+        (kind, start, end)); they are external events, so that inside a
+        graph capture they become event-record nodes of the graph."""
         fg, torch = self.fg, self.torch
 
         def timed(kind, fn):
             if events is None:
                 fn()
                 return
-            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s = torch.cuda.Event(enable_timing=True, external=True)
+            e = torch.cuda.Event(enable_timing=True, external=True)
             s.record()
             fn()
             e.record()
@@ -195,6 +210,19 @@ class PrefillStep:
             timed("quant_128x128", lambda i=i: fg.fp8_quant_128x128_out(self.w[i], self.qb[i], self.sb[i]))
             timed("gemm", lambda i=i: fg.fp8_gemm_dense_out(self.qa, self.sa, self.qb[i], self.sb[i], self.c[i],
                                                             workspace=self.ws))
+
+
+def capture_steps(step, torch, stream, steps):
+    """One CUDA graph holding `steps` steps with a timing event pair around
+    every launch. Returns (graph, events)."""
+    events = []
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(steps):
+                step.run(events)
+    torch.cuda.synchronize()
+    return graph, events
 
 
 # ---------------------------------------------------------------- replicas
@@ -211,6 +239,19 @@ def slowest_replica_ms(total_ms, dist, device):
 def job_throughput(units_per_step, world, ms_per_step):
     """Whole-job rate: the units all `world` replicas processed per second."""
     return units_per_step * world / (ms_per_step * 1e-3)
+
+
+def cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+MIN_WARMUP_S = 1.0  # warm-up wall time floor: clocks and power settle under load
 
 
 def run_ours(args, rank, world, local_rank):
@@ -230,35 +271,87 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
 
     step = PrefillStep(fg, torch, device)
+    stream = torch.cuda.Stream(device=device)
+    stream.wait_stream(torch.cuda.current_stream())
+    # The timed steps, captured once (outside the timed region).
+    with torch.cuda.stream(stream):
+        step.run()  # first calls outside capture: one-time per-device set-up
+    torch.cuda.synchronize()
+    try:
+        graph, events = capture_steps(step, torch, stream, args.steps)
+        per_kernel_timing = "event nodes inside the replayed graph"
+    except RuntimeError as exc:  # event nodes refused in capture: time kernels eagerly instead
+        print(f"note: per-kernel event nodes unavailable in capture ({exc}); timing kernels eagerly",
+              file=sys.stderr)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                for _ in range(args.steps):
+                    step.run()
+        events = None
+        per_kernel_timing = "eager launches with events around each (host gaps included)"
+
     clocks = ClockSampler(local_rank)
     clocks.start()
-    time.sleep(0.3)  # let the sampler start (before the warm-up: no idle gap before the timed steps)
-    for _ in range(args.warmup):
-        step.run()
+    # Warm-up: W eager steps, then more until MIN_WARMUP_S of wall time has
+    # passed (a fixed count of ~1 ms steps leaves the clocks and the power
+    # state of an idle GPU still settling in the timed region).
+    t_warm = time.time()
+    warm_steps = 0
+    with torch.cuda.stream(stream):
+        while warm_steps < args.warmup or time.time() - t_warm < MIN_WARMUP_S:
+            step.run()
+            warm_steps += 1
+            if warm_steps % 50 == 0:
+                stream.synchronize()
+        graph.replay()  # the graph's own first replay is warm-up too
     fg.check()
     barrier()
 
-    events = []
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
     barrier()
     w0 = time.time()
-    start.record()
-    for _ in range(args.steps):
-        step.run(events)
-    end.record()
+    with torch.cuda.stream(stream):
+        start.record()
+        graph.replay()
+        end.record()
     barrier()
     clocks.mark(w0, time.time())
     clocks.stop()
     fg.check()
     total_ms = start.elapsed_time(end)
+    if events is None:
+        events = []
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                step.run(events)
+        barrier()
     per_kind = {}
     for kind, s, e in events:
         per_kind.setdefault(kind, []).append(s.elapsed_time(e))
     total_ms = slowest_replica_ms(total_ms, dist, device)
     ms_per_step = total_ms / args.steps
 
+    # Eager reading of the same steps (launches from the host, no graph):
+    # what a caller that does not capture gets.
+    with torch.cuda.stream(stream):
+        barrier()
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        es.record()
+        for _ in range(args.steps):
+            step.run()
+        ee.record()
+    barrier()
+    eager_ms = es.elapsed_time(ee) / args.steps
+
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(step, fg, torch, device, max(2, min(args.steps, 5)), barrier)
+
+    cfgs = None
+    if not args.no_configs:
+        cfgs = run_configs(fg, torch, device)
 
     if rank != 0:
         if dist is not None:
@@ -299,7 +392,10 @@ def run_ours(args, rank, world, local_rank):
             "M": M_PREFILL, "K": K_PREFILL, "N": list(N_PREFILL),
             "l2": "no flush: each step streams ~1.3 GB (> 126 MB L2)",
             "parallelism": f"replicas x{world}",
+            "timing": "K steps captured in one CUDA graph, replayed once in the timed region",
+            "per_kernel_timing": per_kernel_timing,
         },
+        "eager_ms_per_step": round(eager_ms, 4),
         "roofline": {
             "bound": "tensor",
             "achieved": round(gemm_tflops, 1),
@@ -321,12 +417,16 @@ def run_ours(args, rank, world, local_rank):
             "hbm_peak_gbs": peaks["hbm_gbs"],
             "gemm_per_n_ms": {str(n): round(statistics.mean(per_kind["gemm"][i::len(N_PREFILL)]), 4)
                               for i, n in enumerate(N_PREFILL)},
+            "shares": {k: round(sum(per_kind[k]) / sum(sum(v) for v in per_kind.values()), 4) for k in per_kind},
         },
         "e2e": e2e,
         "gpu_launches": step.launches * args.steps,
         "clocks": clocks.summary(),
         "kernel_sha": sha,
     }
+    line["warmup_done"] = {"steps": warm_steps, "min_seconds": MIN_WARMUP_S}
+    if cfgs is not None:
+        line["configs"] = cfgs
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if dist is not None:
@@ -363,6 +463,53 @@ def run_e2e(step, fg, torch, device, steps, barrier):
     dt = (time.perf_counter() - t0) / steps
     return {"value": round(step.flops / dt / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": round(dt * 1e3, 3), "steps": steps}
+
+
+# Every other workload of the path, graph-timed one kernel at a time
+# (case, shape, requant source). Shapes: decode M in {64, 128} x
+# (N, K) in {(7168, 16384), (4096, 7168)}; grouped-contiguous MoE, 8
+# experts and 8192 Zipf-routed tokens, (N, K) in {(4096, 7168), (7168,
+# 2048)}; grouped-masked MoE, 16 experts of <= 256 tokens, N=4096, K=7168;
+# its weight gradient; the 128x1 requantization from E4M3 and from BF16;
+# and the small dense case.
+CONFIG_CASES = (
+    ("gemm", (128, 256, 512), None),
+    ("gemm", (64, 7168, 16384), None),
+    ("gemm", (128, 7168, 16384), None),
+    ("gemm", (64, 4096, 7168), None),
+    ("gemm", (128, 4096, 7168), None),
+    ("contig", (8, 8192, 4096, 7168), None),
+    ("contig", (8, 8192, 7168, 2048), None),
+    ("masked", (16, 256, 4096, 7168), None),
+    ("wgrad", (16, 256, 4096, 7168), None),
+    ("requant", (4096, 7168), "e4m3"),
+    ("requant", (4096, 7168), "bf16"),
+)
+
+
+def run_configs(fg, torch, device):
+    peaks, src = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_PER_BF16
+    hbm = peaks["hbm_gbs"]
+    out = {}
+    for case, dims, rsrc in CONFIG_CASES:
+        r = time_case(case, dims, rsrc or "e4m3", steps=10, warmup=3, graph_reps=10)
+        name = f"{case}{'_' + rsrc if rsrc else ''} {'x'.join(map(str, dims))}"
+        t = r["ms_median"] * 1e-3
+        ent = {"ms": r["ms_median"], "GB/s": r["GB/s"]}
+        if "TFLOP/s" in r:
+            t_tc = r["flops"] / (fp8_peak * 1e12)
+            t_hbm = r["bytes"] / (hbm * 1e9)
+            ent["TFLOP/s"] = r["TFLOP/s"]
+            ent["bound"] = "tensor" if t_tc >= t_hbm else "hbm"
+            ent["roofline_frac"] = round(max(t_tc, t_hbm) / t, 4)
+        else:
+            ent["bound"] = "hbm"
+            ent["roofline_frac"] = round(r["GB/s"] / hbm, 4)
+        out[name] = ent
+    out["_note"] = (f"graph-timed medians, rotating buffer sets (every call reads HBM); roofline time = "
+                    f"max(flops / {round(fp8_peak, 1)} TFLOP/s, bytes / {hbm} GB/s), {src} peaks")
+    return out
 
 
 # ---------------------------------------------------------------- oracle arm
@@ -410,7 +557,7 @@ def blas_threads():
 def cpu_baseline(seconds=15.0):
     flops, dt, desc = oracle_sample(seconds)
     return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-            "sample": desc, "seconds": round(dt, 2), "host_cpus": os.cpu_count()}
+            "sample": desc, "seconds": round(dt, 2), "host_cpus": os.cpu_count(), "cpu_model": cpu_model()}
 
 
 def run_reference(args, rank, world):
@@ -443,13 +590,13 @@ def run_reference(args, rank, world):
         "config": {"workload": "dense prefill: M=4096, K=7168, N in {2112,24576,7168,4096} (bounded sample)",
                    "M": M_PREFILL, "K": K_PREFILL, "N": list(N_PREFILL)},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-                         "sample": desc},
+                         "sample": desc, "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
 
-def run_case(args):
-    """Time one kernel on one shape (sweeps and ncu captures): prints one JSON line.
+def time_case(case, dims, src="e4m3", steps=20, warmup=5, graph_reps=10, rotate=True, workspace=True):
+    """Time one kernel on one shape through a captured CUDA graph; returns a dict.
 
     gemm M,N,K        dense GEMM, bf16 out (operands quantized once, untimed)
     contig E,T,N,K    grouped-contiguous MoE GEMM: T tokens routed by Zipf(1.1) counts
@@ -463,20 +610,20 @@ def run_case(args):
     import fp8_fine_grained_24_b300 as fg
     import workloads as wl
 
-    dims = [int(v) for v in args.shape.split(",")]
-    dev = torch.device("cuda", 0)
+    dims = [int(v) for v in dims]
+    dev = torch.device("cuda", torch.cuda.current_device())
 
     def make(seed):
         """One independent buffer set: returns (call, algorithmic bytes, flops or None)."""
-        if args.case == "gemm":
+        if case == "gemm":
             M, N, K = dims
             qa, sa = fg.fp8_quant_1x128(wl.activations(M, K, seed, device=dev))
             qb, sb = fg.fp8_quant_128x128(wl.weights((N, K), seed + 1, device=dev))
             c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-            ws = None if args.no_workspace else fg.gemm_workspace(M, N, K, device=dev)
+            ws = None if (not workspace) else fg.gemm_workspace(M, N, K, device=dev)
             return (lambda: fg.fp8_gemm_dense_out(qa, sa, qb, sb, c, workspace=ws),
                     gemm_bytes(M, N, K), gemm_flops(M, N, K))
-        if args.case == "contig":
+        if case == "contig":
             E, T, N, K = dims
             counts = wl.zipf_counts(T, E, 1.1, seed)
             lay = wl.contig_layout(counts)
@@ -487,7 +634,7 @@ def run_case(args):
             c = torch.empty((Mt, N), dtype=torch.bfloat16, device=dev)
             nb = Mt * K + E * N * K + Mt * (K // 128) * 4 + E * (N // 128) * (K // 128) * 4 + T * N * 2
             return (lambda: fg.fp8_gemm_grouped_contig_out(qa, sa, qb, sb, mi, c), nb, 2.0 * T * N * K)
-        if args.case == "masked":
+        if case == "masked":
             E, Mmax, N, K = dims
             counts = wl.masked_counts(E, Mmax, seed)
             qa, sa = fg.fp8_quant_1x128(wl.activations(E * Mmax, K, seed, device=dev))
@@ -502,7 +649,7 @@ def run_case(args):
             nb = T * K + E * N * K + T * N * 2
             return (lambda: fg.fp8_gemm_grouped_masked_out(qa, sa3, qb, sb, mm, c, expected_m=Mmax), nb,
                     2.0 * T * N * K)
-        if args.case == "wgrad":
+        if case == "wgrad":
             # per expert dW_e[N, C] = G_e^T X_e over its valid tokens: operands
             # requantized to 128x1 tiles with power-of-2 scales, FP32 out
             E, Tmax, N, C = dims
@@ -518,38 +665,38 @@ def run_case(args):
             return (lambda: fg.fp8_gemm_grouped_masked_out(qgT, sgT, qxT, sxT, vr, out, b_scale_kind=fg.SCALE_ROW,
                                                            mask_dim=fg.MASK_K, expected_m=Tmax),
                     nb, 2.0 * T * N * C)
-        if args.case == "quant1x128":
+        if case == "quant1x128":
             M, K = dims
             x = wl.activations(M, K, seed, device=dev)
             q = torch.empty((M, K), dtype=torch.uint8, device=dev)
             s = torch.empty((K // 128, fg.scale_ld(M)), dtype=torch.float32, device=dev)
             return lambda: fg.fp8_quant_1x128_out(x, q, s), quant_1x128_bytes(M, K), None
-        if args.case == "quant128x128":
+        if case == "quant128x128":
             N, K = dims
             w = wl.weights((N, K), seed + 1, device=dev)
             q = torch.empty((N, K), dtype=torch.uint8, device=dev)
             s = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=dev)
             return lambda: fg.fp8_quant_128x128_out(w, q, s), quant_128x128_bytes(N, K), None
-        if args.case == "requant":
+        if case == "requant":
             T, C = dims
             x = wl.activations(T, C, seed, device=dev)
             qT = torch.empty((C, T), dtype=torch.uint8, device=dev)
             sT = torch.empty((T // 128, fg.scale_ld(C)), dtype=torch.float32, device=dev)
             out_bytes = T * C + (T // 128) * C * 4
-            if args.src == "e4m3":
+            if src == "e4m3":
                 qa, sa = fg.fp8_quant_1x128(x)
                 return (lambda: fg.fp8_requant_128x1_out(qa.view(torch.float8_e4m3fn), sa, qT, sT, pow2=True),
                         T * C + T * (C // 128) * 4 + out_bytes, None)
-            xs = x if args.src == "bf16" else x.float()
+            xs = x if src == "bf16" else x.float()
             return (lambda: fg.fp8_requant_128x1_out(xs, None, qT, sT, pow2=True),
                     T * C * xs.element_size() + out_bytes, None)
-        raise SystemExit(f"unknown case {args.case}")
+        raise SystemExit(f"unknown case {case}")
 
     # Independent buffer sets, called round robin, so that the working set
     # of consecutive calls exceeds the 126 MB L2 (every call reads from HBM).
     first = make(1001)
     nbytes, work = first[1], first[2]
-    nsets = 1 if args.no_rotate else max(1, min(8, -(-L2_ROTATE_BYTES // max(1, nbytes))))
+    nsets = 1 if not rotate else max(1, min(8, -(-L2_ROTATE_BYTES // max(1, nbytes))))
     fns = [first[0]] + [make(1001 + 10 * i)[0] for i in range(1, nsets)]
     unit = "TFLOP/s" if work is not None else "GB/s"
     calls = [0]
@@ -558,12 +705,12 @@ def run_case(args):
         fns[calls[0] % nsets]()
         calls[0] += 1
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         fn()
     fg.check()
     # R calls captured in one CUDA graph: replays keep host launch overhead
     # out of the per-call device time.
-    reps = -(-max(1, args.graph_reps) // nsets) * nsets  # whole rounds over the buffer sets
+    reps = -(-max(1, graph_reps) // nsets) * nsets  # whole rounds over the buffer sets
     stream = torch.cuda.Stream()
     stream.wait_stream(torch.cuda.current_stream())
     graph = torch.cuda.CUDAGraph()
@@ -577,7 +724,7 @@ def run_case(args):
     graph.replay()
     torch.cuda.synchronize()
     times = []
-    for _ in range(args.steps):
+    for _ in range(steps):
         s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s_.record()
         graph.replay()
@@ -587,11 +734,25 @@ def run_case(args):
     fg.check()
     ms = [a.elapsed_time(b) / reps for a, b in times]
     med = statistics.median(ms)
-    out = {"case": args.case, "shape": dims, "ms_median": round(med, 5), "ms_min": round(min(ms), 5),
+    out = {"case": case, "shape": dims, "ms_median": round(med, 5), "ms_min": round(min(ms), 5),
            "bytes": int(nbytes), "GB/s": round(nbytes / (med * 1e-3) / 1e9, 1), "graph_reps": reps,
            "buffer_sets": nsets}
+    if case == "requant":
+        out["src"] = src
     if work is not None:
+        out["flops"] = work
         out["TFLOP/s"] = round(work / (med * 1e-3) / 1e12, 1)
+    del graph, fns, first
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_case(args):
+    """--case mode: time one kernel on --shape and print one JSON line."""
+    dims = [int(v) for v in args.shape.split(",")]
+    out = time_case(args.case, dims, args.src, args.steps, args.warmup, args.graph_reps,
+                    rotate=not args.no_rotate, workspace=not args.no_workspace)
+    out.pop("flops", None)
     print(json.dumps(out), flush=True)
 
 
@@ -614,6 +775,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the graph-timed entries of the other workloads")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))

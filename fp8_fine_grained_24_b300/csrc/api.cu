@@ -93,6 +93,9 @@ int64_t elem_size(int dtype) {
 
 constexpr int64_t kMaxDim = (1ll << 31) - 1;
 
+}  // namespace
+
+namespace fp8fg {
 int check_gemm_common(const void* A, const void* sA, const void* B, const void* sB, int b_scale_kind, void* C,
                       int out_dtype, int accumulate, int64_t rows, int64_t N, int64_t K) {
   if (rows < 0 || N < 0 || K < 0) return fail(FP8FG_ERR_INVALID_ARG, "negative size");
@@ -113,6 +116,10 @@ int check_gemm_common(const void* A, const void* sA, const void* B, const void* 
     return fail(FP8FG_ERR_MISALIGNED, "sB must be 16-byte aligned (per-row scales) or 4-byte aligned");
   return FP8FG_OK;
 }
+}  // namespace fp8fg
+
+namespace {
+using fp8fg::check_gemm_common;
 
 int run_gemm(const fp8fg::GemmProblem& p, cudaStream_t stream) {
   int err = FP8FG_OK;

@@ -29,6 +29,8 @@
 // the promotion warps; the shared-memory ring lets TMA run S blocks ahead.
 #include <atomic>
 #include <cstdlib>
+#include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -780,38 +782,109 @@ Plan plan_gemm(int mode, int64_t rows, int64_t N, int64_t K, int64_t groups, int
   return p;
 }
 
+// Tensor maps of one launch. Encoding five maps costs host time on every
+// call, and a map depends only on the pointers and sizes below, so launches
+// look them up in a small cache keyed by exactly those fields (a map for a
+// freed and reused address with the same sizes is still the right map).
+struct MapKey {
+  const void* A;
+  const void* B;
+  const void* sA;
+  const void* sB;
+  const void* C;
+  int64_t rows, N, K, groupsA, groupsB, groupsC;
+  int32_t bn, b_row, out_f32, pad;
+};
+
+struct MapSet {
+  CUtensorMap a, b, sa, sb, c;
+};
+
+constexpr int kMapCacheSize = 64;
+
+struct MapCache {
+  std::mutex mu;
+  MapKey key[kMapCacheSize];
+  MapSet maps[kMapCacheSize];
+  int used = 0, next = 0;
+};
+
+MapCache& map_cache() {
+  static MapCache c;
+  return c;
+}
+
+template <int BN>
+bool encode_maps(const GemmProblem& p, MapSet* m) {
+  using C = Cfg<BN>;
+  const int64_t KB = p.K / BK;
+  const int64_t groupsA = (p.mode == kModeMaskedRows || p.mode == kModeMaskedK) ? p.groups : 1;
+  bool ok = make_map(&m->a, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.A, p.K, p.rows, groupsA, p.K, p.rows * p.K, BK, BM,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map(&m->b, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.B, p.K, p.N, p.groupsB, p.K, p.N * p.K, BK, BN,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map(&m->sa, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.sA, p.rows, KB, groupsA, ld4(p.rows) * 4,
+                      KB * ld4(p.rows) * 4, BM, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (p.b_row) {
+    ok = ok && make_map(&m->sb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.sB, p.N, KB, p.groupsB, ld4(p.N) * 4,
+                        KB * ld4(p.N) * 4, BN, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+  } else {
+    m->sb = m->sa;  // unused
+  }
+  const int64_t groupsC = groupsA;
+  if (C::kTmaStore) {
+    const int64_t esz = p.out_f32 ? 4 : 2;
+    ok = ok && make_map(&m->c, p.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.C,
+                        p.N, p.rows, groupsC, p.N * esz, p.rows * p.N * esz, 128 / esz, 32,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    m->c = m->sa;  // unused
+  }
+  return ok;
+}
+
+template <int BN>
+bool get_maps(const GemmProblem& p, MapSet* out) {
+  MapKey k;
+  std::memset(&k, 0, sizeof(k));  // padding bytes take part in the comparison
+  const int64_t groupsA = (p.mode == kModeMaskedRows || p.mode == kModeMaskedK) ? p.groups : 1;
+  k.A = p.A; k.B = p.B; k.sA = p.sA; k.sB = p.b_row ? p.sB : nullptr; k.C = p.C;
+  k.rows = p.rows; k.N = p.N; k.K = p.K; k.groupsA = groupsA; k.groupsB = p.groupsB; k.groupsC = groupsA;
+  k.bn = BN; k.b_row = p.b_row; k.out_f32 = p.out_f32;
+  MapCache& c = map_cache();
+  {
+    std::lock_guard<std::mutex> lock(c.mu);
+    for (int i = 0; i < c.used; ++i) {
+      if (std::memcmp(&c.key[i], &k, sizeof(k)) == 0) {
+        *out = c.maps[i];
+        return true;
+      }
+    }
+  }
+  if (!encode_maps<BN>(p, out)) return false;
+  std::lock_guard<std::mutex> lock(c.mu);
+  const int slot = c.used < kMapCacheSize ? c.used++ : c.next;
+  c.next = (slot + 1) % kMapCacheSize;
+  c.key[slot] = k;
+  c.maps[slot] = *out;
+  return true;
+}
+
 template <int BN>
 cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limit_ns, int debug_skip_fill,
                       int num_sms, cudaStream_t stream, const char** detail) {
   using C = Cfg<BN>;
   const int64_t KB = p.K / BK;
-  const int64_t groupsA = (p.mode == kModeMaskedRows || p.mode == kModeMaskedK) ? p.groups : 1;
-  CUtensorMap tmA, tmB, tmSA, tmSB, tmC;
-  bool ok = make_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.A, p.K, p.rows, groupsA, p.K, p.rows * p.K, BK, BM,
-                     CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.B, p.K, p.N, p.groupsB, p.K, p.N * p.K, BK, BN,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.sA, p.rows, KB, groupsA, ld4(p.rows) * 4,
-                      KB * ld4(p.rows) * 4, BM, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (p.b_row) {
-    ok = ok && make_map(&tmSB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.sB, p.N, KB, p.groupsB, ld4(p.N) * 4,
-                        KB * ld4(p.N) * 4, BN, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
-  } else {
-    tmSB = tmSA;  // unused
-  }
-  const int64_t groupsC = (p.mode == kModeMaskedRows || p.mode == kModeMaskedK) ? p.groups : 1;
-  if (C::kTmaStore) {
-    const int64_t esz = p.out_f32 ? 4 : 2;
-    ok = ok && make_map(&tmC, p.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.C,
-                        p.N, p.rows, groupsC, p.N * esz, p.rows * p.N * esz, 128 / esz, 32,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
-  } else {
-    tmC = tmSA;  // unused
-  }
-  if (!ok) {
+  MapSet ms;
+  if (!get_maps<BN>(p, &ms)) {
     *detail = "cuTensorMapEncodeTiled failed (driver entry point missing or arguments rejected)";
     return cudaErrorInvalidValue;
   }
+  const CUtensorMap& tmA = ms.a;
+  const CUtensorMap& tmB = ms.b;
+  const CUtensorMap& tmSA = ms.sa;
+  const CUtensorMap& tmSB = ms.sb;
+  const CUtensorMap& tmC = ms.c;
   KArgs a;
   a.mode = p.mode;
   a.KB = static_cast<int>(KB);

@@ -58,6 +58,12 @@ size_t gemm_workspace_bytes(int mode, int64_t rows, int64_t N, int64_t K, int64_
 // Record the calling thread's last error message (fp8fg_last_error_string).
 void set_last_error(const char* msg);
 
+// Host-side argument checks shared by the dense GEMM entry points (sizes,
+// enums, null pointers, alignment). Returns FP8FG_OK or an FP8FG_ERR_* code
+// with the message recorded; never touches the GPU.
+int check_gemm_common(const void* A, const void* sA, const void* B, const void* sB, int b_scale_kind, void* C,
+                      int out_dtype, int accumulate, int64_t rows, int64_t N, int64_t K);
+
 // Byte range of a workspace of `workspace_bytes` that must be zero when a
 // launch starts (the arrival counters of the plan that workspace allows);
 // *bytes = 0 when that plan does not split.

@@ -10,22 +10,29 @@
 // library is loaded, exactly how much device memory it will ever hold.
 //
 // This entry point takes the same inputs and outputs as fp8_gemm_dense and
-// no workspace. Its scratch is a fixed array in device memory that the
-// library reserves when it is loaded: 64 MiB on every GPU the process uses,
-// held until the process exits. That covers every dense shape on GPUs with
+// no workspace. Its scratch is a fixed 64 MiB array in device memory, part
+// of this library's device code. That covers every dense shape on GPUs with
 // up to about 170 SMs (the Stream-K scratch holds at most three 128 KB
-// partial tiles per SM plus counters). Nothing here calls
-// cudaMalloc, cudaFree or any routine that allocates.
+// partial tiles per SM plus counters). Nothing here calls cudaMalloc,
+// cudaFree or any routine that allocates.
 //
 // Notes for users:
-//   * The first call on a device does the set-up: it looks up the array's
-//     device address on that device (cudaGetSymbolAddress) and caches it.
-//     That first call should come before any stream capture.
+//   * When the memory is committed: the CUDA runtime loads a library's
+//     device code lazily by default (CUDA_MODULE_LOADING=LAZY), so the
+//     array is committed on a device by the first call of this entry point
+//     there, which looks up its device address (cudaGetSymbolAddress) and
+//     caches it. That first call may therefore fail for lack of device
+//     memory, and it may synchronize the device: make it once at start-up,
+//     outside any latency-critical region and before any stream capture.
+//     From then on the array stays held on that device until the process
+//     exits. (With CUDA_MODULE_LOADING=EAGER it is committed when the
+//     library is loaded.)
 //   * All calls in the process share the one array. Two calls whose GPU work
 //     overlaps (different streams, or different host threads without
 //     ordering) race on it and may produce wrong results: order them.
-//   * A problem whose scratch need exceeds the array is rejected with
-//     FP8FG_ERR_UNSUPPORTED_SHAPE before anything is enqueued.
+//   * Arguments are checked exactly as fp8_gemm_dense checks them, on the
+//     host, before anything is enqueued. A problem whose scratch need
+//     exceeds the array is rejected with FP8FG_ERR_UNSUPPORTED_SHAPE.
 //   * The part of the scratch that must start at zero (the Stream-K arrival
 //     counters) is cleared on the caller's stream by every call.
 #include <mutex>
@@ -85,20 +92,15 @@ extern "C" {
 int fp8_gemm_dense_noalloc(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
                            int b_scale_kind, void* C, int out_dtype, int accumulate, int64_t M, int64_t N,
                            int64_t K, fp8fg_stream_t stream) {
-  auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-  const bool plausible = M > 0 && N > 0 && K > 0 && K % 128 == 0 && N % 8 == 0 && M < (1ll << 31) &&
-                         N < (1ll << 31) && K < (1ll << 31) && A && sA && B && sB && C && a16(A) && a16(B) &&
-                         a16(C) && a16(sA) && (b_scale_kind == FP8FG_SCALE_BLOCK128 || b_scale_kind == FP8FG_SCALE_ROW) &&
-                         (out_dtype == FP8FG_BF16 || out_dtype == FP8FG_FP32) && (accumulate == 0 || accumulate == 1) &&
-                         !(accumulate && out_dtype != FP8FG_FP32) &&
-                         (reinterpret_cast<uintptr_t>(sB) & (b_scale_kind == FP8FG_SCALE_ROW ? 15u : 3u)) == 0;
-  if (!plausible) {
-    // empty or rejected arguments: the dense entry point gives the answer (a
-    // no-op or its error code and message) and nothing is enqueued here
+  if (M == 0 || N == 0) {
+    // empty product: the dense entry point's answer (a no-op, or its error
+    // for negative sizes); nothing is enqueued
     return fp8_gemm_dense(A, sA, B, sB, b_scale_kind, C, out_dtype, accumulate, M, N, K, nullptr, 0, stream);
   }
+  int rc = fp8fg::check_gemm_common(A, sA, B, sB, b_scale_kind, C, out_dtype, accumulate, M, N, K);
+  if (rc != FP8FG_OK) return rc;
   NoallocDevice* d = nullptr;
-  int rc = noalloc_device(&d);
+  rc = noalloc_device(&d);
   if (rc != FP8FG_OK) return rc;
   const size_t need = fp8fg::gemm_workspace_bytes(fp8fg::kModeDense, M, N, K, 1, d->num_sms);
   if (need > kStaticScratchBytes) {

@@ -168,17 +168,22 @@ FP8FG_API int fp8_gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B
  * device memory. (No counterpart in the paper: a deployment convenience of
  * this library.) Some callers only receive device pointers from a host
  * application that owns all device memory and offers no allocator, or run
- * where a device allocation is forbidden; they cannot provide the Stream-K
- * workspace. This entry point computes the same product with the same
- * arguments minus the workspace, using instead a 64 MiB array that the
- * library reserves in device memory when it is loaded (on every GPU the
- * process uses, until exit). It allocates nothing.
- *   - The first call on a device looks up that array's device address;
- *     that first call should come before any stream capture.
+ * where a device allocation is forbidden (it can synchronize the device);
+ * they cannot provide the Stream-K workspace. This entry point computes the
+ * same product with the same arguments minus the workspace, using instead a
+ * 64 MiB array that is part of the library's device code. It allocates
+ * nothing.
+ *   - The CUDA runtime loads device code lazily by default, so the array is
+ *     committed on a device by the first call there (which also looks up its
+ *     address). That first call may fail for lack of device memory or
+ *     synchronize the device: make it at start-up, outside latency-critical
+ *     code and before any stream capture. The array is then held on that
+ *     device until the process exits.
  *   - All calls share the array: calls whose GPU work overlaps race on it.
  *   - Each call clears the part of the array that must start at zero.
- *   - A shape needing more scratch than 64 MiB is rejected with
- *     FP8FG_ERR_UNSUPPORTED_SHAPE (none exists on GPUs with up to ~170 SMs).
+ *   - Arguments are checked as fp8_gemm_dense checks them; a shape needing
+ *     more scratch than 64 MiB is rejected with FP8FG_ERR_UNSUPPORTED_SHAPE
+ *     (none exists on GPUs with up to ~170 SMs).
  */
 FP8FG_API int fp8_gemm_dense_noalloc(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
                                      int b_scale_kind, void* C, int out_dtype, int accumulate,
@@ -228,7 +233,9 @@ FP8FG_API int fp8_gemm_grouped_contig(const uint8_t* A, const float* sA, const u
  *   expert without tokens, unchanged when accumulate is 1).
  *
  *   masked_m   device int32 [E], values in [0, M_max] (ROWS) or [0, K] (K)
- *   expected_m host hint of the typical masked_m (tile-shape choice), or 0
+ *   expected_m host hint of the typical masked_m, >= 0. Reserved: checked
+ *              but not used by this version (the kernel finds the active
+ *              tiles from masked_m on the device, whatever the counts)
  *   accumulate FP32 output only, as in fp8_gemm_dense
  * Requires K % 128 == 0, N % 8 == 0, 16-byte aligned A, B, C.
  */

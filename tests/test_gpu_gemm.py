@@ -152,19 +152,20 @@ def test_contig_zipf_counts(lib):
 
 
 @pytest.mark.slow
-def test_contig_full_sampled(lib):
-    E, tokens, N, K = wl.CONTIG_CASES[0]
+@pytest.mark.parametrize("case", range(len(wl.CONTIG_CASES)))
+def test_contig_full_sampled(lib, case):
+    E, tokens, N, K = wl.CONTIG_CASES[case]
     counts = wl.zipf_counts(tokens, E, 1.1, seed=1004)
     lay = wl.contig_layout(counts)
-    x = wl.activations(lay.m_total, K, 1005, device="cuda")
+    x = wl.activations(lay.m_total, K, 1005 + 10 * case, device="cuda")
     x[torch.from_numpy(lay.m_indices < 0).cuda()] = 0
-    w = wl.weights((E, N, K), 1006, device="cuda")
+    w = wl.weights((E, N, K), 1006 + 10 * case, device="cuda")
     qa_d, sa_d = lib.fp8_quant_1x128(x)
     qb_d, sb_d = lib.fp8_quant_128x128(w)
     c = torch.full((lay.m_total, N), float("nan"), dtype=torch.bfloat16, device="cuda")
     lib.fp8_gemm_grouped_contig_out(qa_d, sa_d, qb_d, sb_d, dev(lay.m_indices), c)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(5)
+    rng = np.random.default_rng(5 + case)
     real_rows = np.flatnonzero(lay.m_indices >= 0)
     rows = np.sort(rng.choice(real_rows, 48, replace=False))
     qa, sa = quant.quant_1x128(to_np32(x[rows]))
@@ -266,6 +267,93 @@ def test_masked_full_decode_sampled(lib):
             compare_gemm(c[e, :m, cols], gemm.gemm_dense(qa, sa, qb, sb), True)
     for e in range(E):
         assert torch.isnan(c[e, int(masked[e]):]).all()
+
+
+# ---------------------------------------------------------------- weight gradients at full size
+@pytest.mark.slow
+def test_wgrad_masked_moe_full_config(lib):
+    # The MoE weight gradient end to end at its full size: 16 experts of at
+    # most 256 tokens, dW_e[4096, 7168] = G_e^T X_e in FP32. X is cached as
+    # 1x128 E4M3 and retiled to 128x1 with power-of-2 scales; the activation
+    # gradient G (BF16) goes straight to 128x1 pow2 tiles. One expert has no
+    # tokens and one a full 256.
+    E, Tmax, N, C = wl.MASKED_CASE
+    counts = wl.masked_counts(E, Tmax, seed=1011)
+    counts[2], counts[7] = 0, Tmax
+    g = wl.normal((E, Tmax, N), 1012, device="cuda", dtype=torch.bfloat16)
+    x = wl.activations(E * Tmax, C, 1013, device="cuda").view(E, Tmax, C)
+    wl.zero_rows_beyond(g, counts, Tmax)
+    wl.zero_rows_beyond(x, counts, Tmax)
+    vr = torch.as_tensor(counts, device="cuda")
+    qx = torch.empty((E, Tmax, C), dtype=torch.uint8, device="cuda")
+    sx = torch.empty((E, C // 128, ld4(Tmax)), dtype=torch.float32, device="cuda")
+    for e in range(E):
+        lib.fp8_quant_1x128_out(x[e], qx[e], sx[e])
+    qxT, sxT = lib.fp8_requant_128x1(qx.view(torch.float8_e4m3fn), sx, vr, pow2=True)
+    qgT, sgT = lib.fp8_requant_128x1(g, None, vr, pow2=True)
+    dw = torch.full((E, N, C), float("nan"), dtype=torch.float32, device="cuda")
+    lib.fp8_gemm_grouped_masked_out(qgT, sgT, qxT, sxT, vr, dw, b_scale_kind=lib.SCALE_ROW,
+                                    mask_dim=lib.MASK_K, expected_m=Tmax)
+    lib.check()
+    assert torch.count_nonzero(dw[2]) == 0, "an expert without tokens must get dW = 0"
+    rng = np.random.default_rng(11)
+    for e in (1, 7, 13):
+        m = int(counts[e])
+        # oracle operands from the generator's values only
+        q_o, s_o = quant.quant_1x128(to_np32(x[e]))
+        qxT_o, sxT_o = quant.requant_128x1(q_o, s_o, m, True)
+        qgT_o, sgT_o = quant.requant_128x1(to_np32(g[e]), None, m, True)
+        assert np.array_equal(qxT[e].cpu().numpy(), qxT_o), f"expert {e}: requantized X differs"
+        assert np.array_equal(qgT[e].cpu().numpy(), qgT_o), f"expert {e}: requantized G differs"
+        for nb, cb in [(0, 0), (N // 128 - 1, C // 128 - 1)] + [tuple(rng.integers(0, (N // 128, C // 128)))
+                                                                  for _ in range(3)]:
+            rows = np.arange(nb * 128, nb * 128 + 128)
+            cols = np.arange(cb * 128, cb * 128 + 128)
+            ref = gemm.wgrad(qgT_o, sgT_o, qxT_o, sxT_o, rows=rows, cols=cols)
+            compare_gemm(dw[e, nb * 128:nb * 128 + 128, cb * 128:cb * 128 + 128], ref, False)
+
+
+@pytest.mark.parametrize("T", [512])
+def test_dense_wgrad_many_tiles_accumulate(lib, T):
+    # Row-scaled B with FP32 output added into a nonzero C: 32 x 28 output
+    # tiles on the SMs, so every CTA runs several tiles (TMEM buffer and
+    # ring phases flip across tiles, TMA reduce-add epilogue under load).
+    N, C = 4096, 7168
+    qgT, sgT, qxT, sxT = _wgrad_operands(T, N, C, 85)
+    base = wl.normal((N, C), 86, device="cuda")
+    out = base.clone()
+    lib.fp8_gemm_dense_out(dev(qgT), dev(pad_rows_scale(sgT, N)), dev(qxT), dev(pad_rows_scale(sxT, C)), out,
+                           b_scale_kind=lib.SCALE_ROW, accumulate=True)
+    lib.check()
+    ref = gemm.wgrad(qgT, sgT, qxT, sxT) + base.double().cpu().numpy()
+    compare_gemm(out, ref, False)
+
+
+@pytest.mark.slow
+def test_dense_wgrad_prefill_tokens_accumulate_sampled(lib):
+    # Dense weight gradient over the 4096 prefill tokens, added into FP32
+    # dW (gradient accumulation): dW[4096, 7168] += G^T X, sampled blocks.
+    T, N, C = 4096, 4096, 7168
+    g = wl.normal((T, N), 1021, device="cuda", dtype=torch.bfloat16)
+    x = wl.activations(T, C, 1022, device="cuda")
+    qx, sx = lib.fp8_quant_1x128(x)
+    qxT, sxT = lib.fp8_requant_128x1(qx.view(torch.float8_e4m3fn), sx, pow2=True)
+    qgT, sgT = lib.fp8_requant_128x1(g, pow2=True)
+    base = wl.normal((N, C), 1023, device="cuda")
+    out = base.clone()
+    lib.fp8_gemm_dense_out(qgT, sgT, qxT, sxT, out, b_scale_kind=lib.SCALE_ROW, accumulate=True)
+    lib.check()
+    rng = np.random.default_rng(12)
+    for nb, cb in [(0, 0), (N // 128 - 1, C // 128 - 1), tuple(rng.integers(0, (N // 128, C // 128)))]:
+        rows = slice(nb * 128, nb * 128 + 128)
+        cols = slice(cb * 128, cb * 128 + 128)
+        # a 128x128 block of dW needs only its 128 channels of G and of X
+        # (one 1x128 group of X, 128x1 tiles down the tokens)
+        q_o, s_o = quant.quant_1x128(to_np32(x[:, cols]))
+        qxT_o, sxT_o = quant.requant_128x1(q_o, s_o, None, True)
+        qgT_o, sgT_o = quant.requant_128x1(to_np32(g[:, rows]), None, None, True)
+        ref = gemm.wgrad(qgT_o, sgT_o, qxT_o, sxT_o) + base[rows, cols].double().cpu().numpy()
+        compare_gemm(out[rows, cols], ref, False)
 
 
 # ---------------------------------------------------------------- bounded waits

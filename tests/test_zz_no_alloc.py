@@ -2,21 +2,24 @@
 
 Some callers only hold device pointers handed to them (no allocator), so they
 cannot pass the split-K workspace that fp8_gemm_dense asks for on
-decode-sized shapes. The no-allocation entry point uses a scratch array the
-library reserves when it is loaded instead. This test calls it through the C
-ABI and checks its output against the existing fp8_gemm_dense entry point
-(given a caller workspace) on the same inputs, on two calls in a row (the
-shared scratch must be left usable), within the GEMM tolerance the other GPU
-tests use. The file sorts last so that a run stopping at the first failure
-has already run every other test.
+decode-sized shapes. The no-allocation entry point uses a fixed scratch array
+inside the library instead. These tests call it through the C ABI and check
+its output against the oracle's FP64 product of the same (oracle-quantized)
+operands, within the GEMM tolerance the other GPU tests use, on two calls in
+a row (the shared scratch must be left usable by the first call). Shapes that
+split K are asserted to need scratch, so the static array is really used.
+The file sorts last so that a run stopping at the first failure has already
+run every other test.
 """
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
 import workloads as wl
-from parity import compare_gemm
+from oracle import gemm, quant
+from parity import compare_gemm, dev, pad_rows_scale, to_np32
 
 pytestmark = pytest.mark.gpu
 
@@ -33,22 +36,34 @@ def _p(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
-@pytest.mark.parametrize("M,N,K,out_dtype", [
-    (64, 4096, 7168, torch.bfloat16),    # splits K: uses the static scratch
-    (128, 7168, 2048, torch.bfloat16),   # splits K
-    (64, 520, 2048, torch.float32),      # splits K, FP32 output
-    (512, 1024, 1024, torch.bfloat16),   # enough tiles: no split, no scratch
+def _operands(M, N, K, seed, col_blocks):
+    """Oracle-quantized A (all rows) and B (all rows), plus the oracle's
+    FP64 product restricted to the given 128-column blocks of C."""
+    x = wl.activations(M, K, seed, device="cpu")
+    w = wl.weights((N, K), seed + 1, device="cpu")
+    qa, sa = quant.quant_1x128(to_np32(x))
+    qb, sb = quant.quant_128x128(to_np32(w))
+    refs = {}
+    for nb in col_blocks:
+        cols = slice(nb * 128, min(N, nb * 128 + 128))
+        refs[nb] = gemm.gemm_dense(qa, sa, qb[cols], sb[nb:nb + 1])
+    return dev(qa), dev(pad_rows_scale(sa, M)), dev(qb), dev(sb), refs
+
+
+@pytest.mark.parametrize("M,N,K,out_dtype,splits", [
+    (64, 4096, 7168, torch.bfloat16, True),    # splits K: uses the static scratch
+    (128, 7168, 2048, torch.bfloat16, True),   # splits K
+    (64, 520, 2048, torch.float32, True),      # splits K, FP32 output
+    (512, 1024, 1024, torch.bfloat16, False),  # enough tiles: no split, no scratch
 ])
-def test_noalloc_matches_dense_entry(lib, M, N, K, out_dtype):
+def test_noalloc_matches_oracle(lib, M, N, K, out_dtype, splits):
     fg = lib
     f = _entry(fg)
-    x = wl.activations(M, K, 9100 + M, device="cuda")
-    w = wl.weights((N, K), 9200 + N, device="cuda")
-    qa, sa = fg.fp8_quant_1x128(x)
-    qb, sb = fg.fp8_quant_128x128(w)
-    ref = fg.fp8_gemm_dense(qa, sa, qb, sb, out_dtype=out_dtype)  # existing entry point, caller workspace
-    torch.cuda.synchronize()
-    ref_np = ref.double().cpu().numpy()
+    need = fg.gemm_workspace_size(M, N, K)
+    assert (need > 0) == splits, f"scratch need {need} bytes for {M}x{N}x{K}"
+    nbl = (N + 127) // 128
+    blocks = sorted({0, nbl // 2, nbl - 1})
+    qa, sa, qb, sb, refs = _operands(M, N, K, 9100 + M + N, blocks)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     code = fg.FP32 if out_dtype == torch.float32 else fg.BF16
     for _ in range(2):
@@ -56,7 +71,29 @@ def test_noalloc_matches_dense_entry(lib, M, N, K, out_dtype):
         rc = f(_p(qa), _p(sa), _p(qb), _p(sb), fg.SCALE_BLOCK128, _p(c), code, 0, M, N, K, stream)
         assert rc == 0, fg.lib.fp8fg_last_error_string().decode()
         fg.check()
-        compare_gemm(c, ref_np, out_dtype == torch.bfloat16)
+        for nb, ref in refs.items():
+            compare_gemm(c[:, nb * 128:min(N, nb * 128 + 128)], ref, out_dtype == torch.bfloat16)
+
+
+def test_noalloc_fp32_accumulate_matches_oracle(lib):
+    # C += A B^T into a nonzero FP32 C: with K split, the last piece of each
+    # tile adds the summed partials into C
+    fg = lib
+    f = _entry(fg)
+    M, N, K = 64, 1792, 6912
+    assert fg.gemm_workspace_size(M, N, K) > 0
+    blocks = [0, 7, 13]
+    qa, sa, qb, sb, refs = _operands(M, N, K, 9301, blocks)
+    c0 = wl.normal((M, N), 9302, device="cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for _ in range(2):
+        c = c0.clone()
+        rc = f(_p(qa), _p(sa), _p(qb), _p(sb), fg.SCALE_BLOCK128, _p(c), fg.FP32, 1, M, N, K, stream)
+        assert rc == 0, fg.lib.fp8fg_last_error_string().decode()
+        fg.check()
+        for nb, ref in refs.items():
+            cols = slice(nb * 128, nb * 128 + 128)
+            compare_gemm(c[:, cols], ref + c0[:, cols].double().cpu().numpy(), False)
 
 
 def test_noalloc_rejects_bad_arguments_without_enqueueing(lib):
@@ -67,4 +104,5 @@ def test_noalloc_rejects_bad_arguments_without_enqueueing(lib):
     assert rc == fg.ERR_UNSUPPORTED_SHAPE
     rc = f(_p(good), _p(good), _p(good), _p(good), 0, _p(good), fg.BF16, 1, 64, 128, 128, None)
     assert rc == fg.ERR_INVALID_ARG
+    assert f(None, None, None, None, 0, None, fg.BF16, 0, 0, 128, 128, None) == fg.OK
     fg.check()
