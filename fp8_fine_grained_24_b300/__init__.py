@@ -89,6 +89,7 @@ _SIGS = {
     "fp8fg_debug_set": (_c_int, [_c_int, _c_i64]),
     "fp8_gemm_dense_noalloc": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_int, _c_int, _c_i64, _c_i64,
                                         _c_i64, _c_vp]),
+    "fp8fg_study_mma_accumulation": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_vp]),
 }
 
 
@@ -267,10 +268,21 @@ def fp8_gemm_grouped_masked(a, sa, b, sb, masked_m, out_dtype=torch.bfloat16, b_
                                        stream)
 
 
+# ---------------------------------------------------------------- studies
+def study_mma_accumulation(a, b, interval, stream=None):
+    """D[128, N] = a[128, K] b[N, K]^T on unscaled E4M3 codes (uint8), the
+    tensor-core accumulator restarted every `interval` K (see fp8fg.h)."""
+    assert a.shape[0] == 128 and a.shape[1] == b.shape[1]
+    d = torch.empty((128, b.shape[0]), dtype=torch.float32, device=a.device)
+    _check(lib.fp8fg_study_mma_accumulation(_ptr(_as_u8(a)), _ptr(_as_u8(b)), _ptr(d), b.shape[0], a.shape[1],
+                                            int(interval), _stream(stream)))
+    return d
+
+
 __all__ = [
     "lib", "LIB_PATH", "Fp8fgError", "scale_ld", "version", "check", "debug_set",
     "fp8_quant_1x128", "fp8_quant_1x128_out", "fp8_quant_128x128", "fp8_quant_128x128_out",
     "fp8_requant_128x1", "fp8_requant_128x1_out", "gemm_workspace_size", "gemm_workspace",
     "fp8_gemm_dense", "fp8_gemm_dense_out", "fp8_gemm_grouped_contig", "fp8_gemm_grouped_contig_out",
-    "fp8_gemm_grouped_masked", "fp8_gemm_grouped_masked_out",
+    "fp8_gemm_grouped_masked", "fp8_gemm_grouped_masked_out", "study_mma_accumulation",
 ]

@@ -304,6 +304,24 @@ int fp8fg_check(fp8fg_stream_t stream) {
   return FP8FG_OK;
 }
 
+int fp8fg_study_mma_accumulation(const uint8_t* A, const uint8_t* B, float* D, int64_t N, int64_t K,
+                                 int64_t interval, fp8fg_stream_t stream) {
+  if (N < 0 || K < 0 || interval <= 0) return fail(FP8FG_ERR_INVALID_ARG, "negative size or interval <= 0");
+  if (K % 128 != 0 || N % 128 != 0 || interval % 32 != 0)
+    return fail(FP8FG_ERR_UNSUPPORTED_SHAPE, "K and N must be multiples of 128, interval a multiple of 32");
+  if (N == 0 || K == 0) return FP8FG_OK;
+  if (N > kMaxDim || K > kMaxDim) return fail(FP8FG_ERR_UNSUPPORTED_SHAPE, "dimension too large");
+  if (!A || !B || !D) return fail(FP8FG_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(A) || !aligned16(B) || !aligned16(D)) return fail(FP8FG_ERR_MISALIGNED, "A, B, D must be 16-byte aligned");
+  int err = FP8FG_OK;
+  const DeviceState* st = device_state(&err);
+  if (!st) return err;
+  const char* detail = "";
+  cudaError_t e = fp8fg::launch_mma_accum_study(A, B, D, N, K, interval, st->status, g_wait_limit_ns.load(),
+                                                reinterpret_cast<cudaStream_t>(stream), &detail);
+  return e == cudaSuccess ? FP8FG_OK : cuda_fail(e, detail);
+}
+
 int fp8fg_debug_set(int key, int64_t value) {
   switch (key) {
     case 1:

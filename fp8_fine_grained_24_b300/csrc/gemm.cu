@@ -661,14 +661,18 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       bool staged = false;
       if (store) {
         if constexpr (kStage) {
-          uint8_t* region;
+          // Staging area: the first kBorrowWarps warps borrow the stage they
+          // kept from the tile's last K block; the others own a dedicated
+          // area. A tile without K blocks (an expert with no tokens in the
+          // masked-K layout) kept no stage: those warps store row by row.
+          uint8_t* region = nullptr;
           if (held >= 0 && ew < 2)
             region = smem + C::kOffA + held * C::kABytes + ew * C::kEpiWarpBytes;
           else if (held >= 0)
             region = smem + C::kOffB + held * C::kBBytes + (ew - 2) * C::kEpiWarpBytes;
-          else
+          else if (ew >= C::kBorrowWarps)
             region = smem + C::kOffEpi + (ew - C::kBorrowWarps) * C::kEpiWarpBytes;
-          staged = store_tile_tma<NC, kF32>(a, ti, row_in_tile, col0, lane, region, &tmC, acc);
+          if (region != nullptr) staged = store_tile_tma<NC, kF32>(a, ti, row_in_tile, col0, lane, region, &tmC, acc);
         }
         if (!staged) store_row<NC, kF32>(a, ti, row_in_tile, col0, acc);
       }

@@ -259,6 +259,25 @@ FP8FG_API const char* fp8fg_last_error_string(void);
 FP8FG_API const char* fp8fg_version(void);
 
 /*
+ * fp8fg_study_mma_accumulation -- measurement of the tensor core's own FP8
+ * accumulation (no counterpart on the GEMM path; the DeepSeek-V3 report
+ * excerpt, page 1 paragraph 1 and page 2 paragraph 1, measured the H800's:
+ * about 14 bits kept, ~2% error at K=4096 without promotion).
+ *
+ *   A        [128][K] E4M3 codes, used unscaled (scale 1)
+ *   B        [N][K]   E4M3 codes, unscaled
+ *   D        [128][N] float, written: sum over k of A[m][k] * B[n][k], where
+ *            the tensor-core accumulator restarts every `interval` K
+ *            elements and each restarted partial is added into FP32 (IEEE
+ *            round-to-nearest add). interval >= K: one chained accumulator
+ *            (no promotion); 128: the GEMM path's promotion interval.
+ * Requires K % 128 == 0, N % 128 == 0, interval % 32 == 0 (> 0), 16-byte
+ * aligned pointers. Slow by design (one CTA per 128 columns, serial).
+ */
+FP8FG_API int fp8fg_study_mma_accumulation(const uint8_t* A, const uint8_t* B, float* D, int64_t N, int64_t K,
+                                           int64_t interval, fp8fg_stream_t stream);
+
+/*
  * fp8fg_debug_set -- test hooks (no counterpart in the method):
  *   key 1: wait limit of the bounded device waits, in nanoseconds (value 0
  *          restores the default of 2 s);

@@ -219,10 +219,15 @@ def test_masked_decode_like(lib):
     _masked_case(lib, 6, 256, 512, 1024, masked, 53)
 
 
-def test_masked_k_wgrad(lib):
+@pytest.mark.parametrize("E,T,N,C,masked", [
+    (3, 384, 136, 264, (0, 100, 384)),
+    # 256 tiles: CTAs run an empty expert's tile and then a real one, so an
+    # empty tile's epilogue overlaps the next tile's operand loads
+    (4, 256, 1024, 2048, (0, 256, 100, 0)),
+])
+def test_masked_k_wgrad(lib, E, T, N, C, masked):
     # per expert dW_e[N, C] = G_e^T X_e over the expert's tokens (K = tokens)
-    E, T, N, C = 3, 384, 136, 264
-    masked = np.array([0, 100, 384], np.int32)
+    masked = np.array(masked, np.int32)
     qg, sg, qx, sx = [], [], [], []
     for e in range(E):
         a, b, c_, d = _wgrad_operands(T, N, C, 60 + e, valid=masked[e])
