@@ -332,6 +332,10 @@ int fp8fg_debug_set(int key, int64_t value) {
       if (value < -1 || value > 0x7FFFFFFF) return fail(FP8FG_ERR_INVALID_ARG, "bad fill index");
       g_debug_skip_fill.store(static_cast<int>(value));
       return FP8FG_OK;
+    case 3:
+      if (value != 0 && value != 1) return fail(FP8FG_ERR_INVALID_ARG, "value must be 0 or 1");
+      fp8fg::set_pair_gemm_enabled(value == 1);
+      return FP8FG_OK;
     default:
       return fail(FP8FG_ERR_INVALID_ARG, "unknown debug key %d", key);
   }

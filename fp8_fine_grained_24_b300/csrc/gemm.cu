@@ -33,6 +33,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "gemm_common.cuh"
 #include "kernels.h"
 #include "launch.h"
 #include "tmap.h"
@@ -41,8 +42,8 @@ namespace fp8fg {
 
 namespace {
 
-constexpr int BM = 128;
-constexpr int BK = 128;
+using namespace gemm_detail;
+
 constexpr int kContigBand = 16;  // M blocks per raster band of the grouped-contiguous layout
 
 // Tile configurations. The epilogue warps split the tile's columns in
@@ -100,42 +101,6 @@ struct Cfg {
   static_assert((kOffB % 1024) == 0 && (kABytes % 1024) == 0 && (kBBytes % 1024) == 0,
                 "128-byte swizzled tiles need 1024-byte alignment");
   static_assert(!kTmaStore || (kOffEpi % 1024) == 0, "swizzled store boxes need 1024-byte alignment");
-};
-
-struct KArgs {
-  int mode;
-  int rows, N, K;
-  int tiles_m, tiles_n, num_tiles;
-  int groupsB;
-  int accumulate;
-  const int32_t* m_indices;
-  const int32_t* masked;
-  const float* sB;
-  int sb_nblk, sb_kblk;
-  void* C;
-  int64_t ldc;
-  int64_t c_group_stride;
-  uint32_t* status;
-  uint64_t wait_limit_ns;
-  int debug_skip_fill;
-  // Stream-K (dense only, the kSplit variant): tiles [0, dp_tiles) run
-  // whole, tile t on CTA t % gridDim.x; the K blocks of tiles sk_tile0 ..
-  // are sk_units "units" in tile-major order and CTA c takes units
-  // [c * sk_per_cta, (c + 1) * sk_per_cta). A tile whose units fall to
-  // several CTAs is summed, in piece order, by the last piece to arrive,
-  // from FP32 partials in ws_partial (one slot per segment, see reduce_sk).
-  int KB;
-  int dp_tiles;
-  int sk_tile0;                      // first split tile (the tiles before it run whole)
-  int sk_units, sk_per_cta, sk_lcm;  // the planner keeps them below 2^31
-  float* ws_partial;
-  int* ws_count;
-};
-
-struct Tile {
-  int gA, gB, gC, m0, n0, kb0, kbc, tile;
-  int sk_start;  // Stream-K segment: its first unit; -1 for a whole tile
-  bool skip;
 };
 
 template <int BN>
@@ -266,110 +231,6 @@ __device__ __forceinline__ bool work_next(const KArgs& a, Work& w, Tile& ti) {
   return false;
 }
 
-// Convert and store one epilogue thread's share of a tile row.
-template <int NC, bool kF32>
-__device__ __forceinline__ void store_row(const KArgs& a, const Tile& ti, int row_in_tile, int col0,
-                                          const float (&acc)[NC]) {
-  const int row = ti.m0 + row_in_tile;
-  if (row >= a.rows) return;
-  if (a.mode == kModeContig && __ldg(a.m_indices + row) < 0) return;
-  if (a.mode == kModeMaskedRows && row >= __ldg(a.masked + ti.gC)) return;
-  const int ncol = a.N - (ti.n0 + col0);  // a multiple of 8 (N % 8 == 0)
-  const int64_t off = static_cast<int64_t>(ti.gC) * a.c_group_stride + static_cast<int64_t>(row) * a.ldc +
-                      ti.n0 + col0;
-  if constexpr (kF32) {
-    float* c = static_cast<float*>(a.C) + off;
-#pragma unroll
-    for (int j = 0; j < NC; j += 4) {
-      if (j < ncol) {
-        float4 v = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-        if (a.accumulate) {
-          const float4 o = *reinterpret_cast<const float4*>(c + j);
-          v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
-        }
-        *reinterpret_cast<float4*>(c + j) = v;
-      }
-    }
-  } else {
-    __nv_bfloat16* c = static_cast<__nv_bfloat16*>(a.C) + off;
-#pragma unroll
-    for (int j = 0; j < NC; j += 8) {
-      if (j < ncol) {
-        uint4 v;
-        v.x = pack_bf16x2(acc[j], acc[j + 1]);
-        v.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
-        v.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
-        v.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
-        *reinterpret_cast<uint4*>(c + j) = v;
-      }
-    }
-  }
-}
-
-// Tile rows of one epilogue warp (32 rows x NC columns) through its 8 KB
-// shared-memory staging area and TMA stores, when every row of the warp may
-// be written (dense: rows past M are clipped by the tensor map; grouped
-// layouts: no padding or masked rows among the 32). Returns false, having
-// done nothing, otherwise; the caller then stores row by row.
-// Staging: two boxes of 32 rows x 128 bytes (BF16: 64 columns each; FP32:
-// 32 columns each, so FP32 goes out in two rounds of 64 columns) with the
-// 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r % 8)): a warp's
-// 16-byte writes of one chunk index hit 8 distinct chunks, conflict free.
-// FP32 with accumulate adds into C with the TMA reduce-add.
-template <int NC, bool kF32>
-__device__ __forceinline__ bool store_tile_tma(const KArgs& a, const Tile& ti, int row_in_tile, int col0, int lane,
-                                               uint8_t* region, const CUtensorMap* tmC, const float (&acc)[NC]) {
-  const int row = ti.m0 + row_in_tile;
-  bool ok = true;
-  if (a.mode == kModeContig) ok = row < a.rows && __ldg(a.m_indices + row) >= 0;
-  if (a.mode == kModeMaskedRows) ok = row < __ldg(a.masked + ti.gC);
-  if (!__all_sync(0xffffffffu, ok)) return false;
-  constexpr int kColsPerRound = 64;          // two 128-byte boxes
-  constexpr int kBoxCols = kF32 ? 32 : 64;
-  const int y = ti.m0 + (row_in_tile & ~31);
-#pragma unroll
-  for (int rd = 0; rd < NC / kColsPerRound; rd += (kF32 ? 1 : 2)) {
-    // the previous stores must have read the staging area, and the tensor
-    // core's reads of a borrowed stage come before these writes
-    if (lane == 0) bulk_wait_read_all();
-    fence_async_shared();
-    __syncwarp();
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint4 v;
-        if constexpr (kF32) {
-          const int j = rd * kColsPerRound + b * kBoxCols + c * 4;
-          v = make_uint4(__float_as_uint(acc[j]), __float_as_uint(acc[j + 1]), __float_as_uint(acc[j + 2]),
-                         __float_as_uint(acc[j + 3]));
-        } else {
-          const int j = b * kBoxCols + c * 8;
-          v.x = pack_bf16x2(acc[j], acc[j + 1]);
-          v.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
-          v.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
-          v.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
-        }
-        *reinterpret_cast<uint4*>(region + b * 4096 + lane * 128 + ((c ^ (lane & 7)) << 4)) = v;
-      }
-    }
-    fence_async_shared();
-    __syncwarp();
-    if (lane == 0) {
-#pragma unroll
-      for (int b = 0; b < 2; ++b) {
-        const int x = ti.n0 + col0 + (kF32 ? rd * kColsPerRound : 0) + b * kBoxCols;
-        if (kF32 && a.accumulate)
-          tma_reduce_add_3d(tmC, smem_u32(region + b * 4096), x, y, ti.gC);
-        else
-          tma_store_3d(tmC, smem_u32(region + b * 4096), x, y, ti.gC);
-      }
-      bulk_commit();
-    }
-  }
-  return true;
-}
-
 // Stream-K slots: segments are numbered in unit order; a segment starting
 // at unit s is preceded by the tile boundaries (multiples of KB) and CTA
 // boundaries (multiples of sk_per_cta) in (0, s], counted by inclusion-
@@ -422,28 +283,6 @@ __device__ __forceinline__ bool sk_reduce(const KArgs& a, const Tile& ti, int ro
     }
   }
   return true;
-}
-
-// acc[j] += partial[j] * sc  (block-scaled B)   or
-// acc[j] += partial[j] * sbv[j] * sa            (per-row B scales)
-template <int W, bool kBRow>
-__device__ __forceinline__ void promote(float* acc, const uint32_t (&r)[W], float sc, float sa, const float* sbv) {
-  // Pairs of columns on the packed f32x2 pipe: each element still gets one
-  // IEEE round-to-nearest FMA (and, for per-row B scales, one multiply).
-#pragma unroll
-  for (int j = 0; j < W; j += 2) {
-    const uint64_t p = pk2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
-    uint64_t a2 = pk2(acc[j], acc[j + 1]);
-    if constexpr (kBRow) {
-      const float2 b = *reinterpret_cast<const float2*>(sbv + j);
-      a2 = fma2(mul2(p, pk2(b.x, b.y)), pk2(sa, sa), a2);
-    } else {
-      a2 = fma2(p, pk2(sc, sc), a2);
-    }
-    const float2 f = unpk2(a2);
-    acc[j] = f.x;
-    acc[j + 1] = f.y;
-  }
 }
 
 template <int BN, bool kBRow, bool kF32, bool kSplit, bool kCompact>
@@ -699,7 +538,6 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
-int64_t ld4(int64_t r) { return (r + 3) / 4 * 4; }
 
 // Raise the kernel's dynamic shared-memory limit once per device (the call
 // costs tens of microseconds of host time, so it is not repeated per launch).
@@ -786,38 +624,6 @@ Plan plan_gemm(int mode, int64_t rows, int64_t N, int64_t K, int64_t groups, int
   return p;
 }
 
-// Tensor maps of one launch. Encoding five maps costs host time on every
-// call, and a map depends only on the pointers and sizes below, so launches
-// look them up in a small cache keyed by exactly those fields (a map for a
-// freed and reused address with the same sizes is still the right map).
-struct MapKey {
-  const void* A;
-  const void* B;
-  const void* sA;
-  const void* sB;
-  const void* C;
-  int64_t rows, N, K, groupsA, groupsB, groupsC;
-  int32_t bn, b_row, out_f32, pad;
-};
-
-struct MapSet {
-  CUtensorMap a, b, sa, sb, c;
-};
-
-constexpr int kMapCacheSize = 64;
-
-struct MapCache {
-  std::mutex mu;
-  MapKey key[kMapCacheSize];
-  MapSet maps[kMapCacheSize];
-  int used = 0, next = 0;
-};
-
-MapCache& map_cache() {
-  static MapCache c;
-  return c;
-}
-
 template <int BN>
 bool encode_maps(const GemmProblem& p, MapSet* m) {
   using C = Cfg<BN>;
@@ -854,23 +660,10 @@ bool get_maps(const GemmProblem& p, MapSet* out) {
   const int64_t groupsA = (p.mode == kModeMaskedRows || p.mode == kModeMaskedK) ? p.groups : 1;
   k.A = p.A; k.B = p.B; k.sA = p.sA; k.sB = p.b_row ? p.sB : nullptr; k.C = p.C;
   k.rows = p.rows; k.N = p.N; k.K = p.K; k.groupsA = groupsA; k.groupsB = p.groupsB; k.groupsC = groupsA;
-  k.bn = BN; k.b_row = p.b_row; k.out_f32 = p.out_f32;
-  MapCache& c = map_cache();
-  {
-    std::lock_guard<std::mutex> lock(c.mu);
-    for (int i = 0; i < c.used; ++i) {
-      if (std::memcmp(&c.key[i], &k, sizeof(k)) == 0) {
-        *out = c.maps[i];
-        return true;
-      }
-    }
-  }
+  k.kind = BN; k.b_row = p.b_row; k.out_f32 = p.out_f32;
+  if (map_cache_find(k, out)) return true;
   if (!encode_maps<BN>(p, out)) return false;
-  std::lock_guard<std::mutex> lock(c.mu);
-  const int slot = c.used < kMapCacheSize ? c.used++ : c.next;
-  c.next = (slot + 1) % kMapCacheSize;
-  c.key[slot] = k;
-  c.maps[slot] = *out;
+  map_cache_put(k, *out);
   return true;
 }
 
@@ -987,6 +780,47 @@ int pick_bn(int mode, int64_t rows) {
 
 }  // namespace
 
+namespace gemm_detail {
+
+namespace {
+constexpr int kMapCacheSize = 64;
+
+struct MapCache {
+  std::mutex mu;
+  MapKey key[kMapCacheSize];
+  MapSet maps[kMapCacheSize];
+  int used = 0, next = 0;
+};
+
+MapCache& map_cache() {
+  static MapCache c;
+  return c;
+}
+}  // namespace
+
+bool map_cache_find(const MapKey& k, MapSet* out) {
+  MapCache& c = map_cache();
+  std::lock_guard<std::mutex> lock(c.mu);
+  for (int i = 0; i < c.used; ++i) {
+    if (std::memcmp(&c.key[i], &k, sizeof(k)) == 0) {
+      *out = c.maps[i];
+      return true;
+    }
+  }
+  return false;
+}
+
+void map_cache_put(const MapKey& k, const MapSet& m) {
+  MapCache& c = map_cache();
+  std::lock_guard<std::mutex> lock(c.mu);
+  const int slot = c.used < kMapCacheSize ? c.used++ : c.next;
+  c.next = (slot + 1) % kMapCacheSize;
+  c.key[slot] = k;
+  c.maps[slot] = m;
+}
+
+}  // namespace gemm_detail
+
 size_t gemm_workspace_bytes(int mode, int64_t rows, int64_t N, int64_t K, int64_t groups, int num_sms) {
   const Plan plan = plan_gemm(mode, rows, N, K, groups, num_sms, pick_bn(mode, rows), SIZE_MAX);
   return plan.sk ? plan.partial_bytes + plan.count_bytes : 0;
@@ -1001,6 +835,7 @@ void gemm_workspace_zero_range(int mode, int64_t rows, int64_t N, int64_t K, int
 
 cudaError_t launch_gemm(const GemmProblem& p, uint32_t* status, uint64_t wait_limit_ns, int debug_skip_fill,
                         int num_sms, cudaStream_t stream, const char** detail) {
+  if (pair_gemm_eligible(p, num_sms)) return launch_gemm_pair(p, status, wait_limit_ns, debug_skip_fill, stream, detail);
   switch (pick_bn(p.mode, p.rows)) {
     case 192: return launch_bn<192>(p, status, wait_limit_ns, debug_skip_fill, num_sms, stream, detail);
     case 256: return launch_bn<256>(p, status, wait_limit_ns, debug_skip_fill, num_sms, stream, detail);

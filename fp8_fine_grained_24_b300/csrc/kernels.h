@@ -75,6 +75,14 @@ void gemm_workspace_zero_range(int mode, int64_t rows, int64_t N, int64_t K, int
 cudaError_t launch_gemm(const GemmProblem& p, uint32_t* status, uint64_t wait_limit_ns, int debug_skip_fill,
                         int num_sms, cudaStream_t stream, const char** detail);
 
+// The CTA-pair GEMM (gemm_pair.cu): taken for dense problems large enough to
+// fill the GPU with 256 x 256 tiles (pair_gemm_eligible); launch_gemm
+// dispatches to it.
+bool pair_gemm_eligible(const GemmProblem& p, int num_sms);
+void set_pair_gemm_enabled(bool on);
+cudaError_t launch_gemm_pair(const GemmProblem& p, uint32_t* status, uint64_t wait_limit_ns, int debug_skip_fill,
+                             cudaStream_t stream, const char** detail);
+
 // Tensor-core accumulation study (see study.cu): D[128][N] = A[128][K] B[N][K]^T
 // on unscaled E4M3 codes, the MMA accumulator restarted every `interval` K.
 cudaError_t launch_mma_accum_study(const uint8_t* A, const uint8_t* B, float* D, int64_t N, int64_t K,

@@ -384,6 +384,62 @@ def test_timeout_reports_error_and_context_survives(lib):
     compare_gemm(c, gemm.gemm_dense(qa, sa, qb, sb), True)
 
 
+# ---------------------------------------------------------------- CTA pairs (large dense problems)
+# Dense problems whose 128 x 256 tiles outnumber half the SMs run on CTA
+# pairs (tcgen05 cta_group::2, 256 x 256 tiles). Debug key 3 switches the
+# pair kernel off, so both kernels can be checked on the same shapes.
+PAIR_SHAPES = [
+    (1000, 2600, 1024, torch.bfloat16),   # ragged: the last pair tile's peer rows and B half partly out of range
+    (2048, 2560, 2048, torch.float32),
+    (512, 7168, 512, torch.bfloat16),
+]
+
+
+@pytest.mark.parametrize("pair", [1, 0])
+@pytest.mark.parametrize("M,N,K,out_dtype", PAIR_SHAPES)
+def test_pair_and_single_cta_kernels_match_oracle(lib, M, N, K, out_dtype, pair):
+    assert -(-M // 128) * -(-N // 256) * 2 > 148  # large enough for the pair kernel on 148 SMs
+    try:
+        lib.debug_set(3, pair)
+        _dense_case(lib, M, N, K, seed=M + N + K, out_dtype=out_dtype)
+    finally:
+        lib.debug_set(3, 1)
+
+
+def test_pair_kernel_row_scaled_accumulate(lib):
+    # the weight-gradient form on CTA pairs: per-row B scales, FP32 C +=
+    T, N, C = 384, 1024, 2560
+    qgT, sgT, qxT, sxT = _wgrad_operands(T, N, C, 87)
+    base = wl.normal((N, C), 88, device="cuda")
+    out = base.clone()
+    lib.fp8_gemm_dense_out(dev(qgT), dev(pad_rows_scale(sgT, N)), dev(qxT), dev(pad_rows_scale(sxT, C)), out,
+                           b_scale_kind=lib.SCALE_ROW, accumulate=True)
+    lib.check()
+    compare_gemm(out, gemm.wgrad(qgT, sgT, qxT, sxT) + base.double().cpu().numpy(), False)
+
+
+def test_pair_kernel_timeout_reports_error_and_context_survives(lib):
+    M, N, K = 1024, 4096, 512
+    x = wl.activations(M, K, 73, device="cpu")
+    w = wl.weights((N, K), 74, device="cpu")
+    qa, sa, qa_d, sa_d = _quant_a(x)
+    qb, sb, qb_d, sb_d = _quant_b(w)
+    lib.check()
+    try:
+        lib.debug_set(1, 50_000_000)   # 50 ms wait limit
+        lib.debug_set(2, 1)            # every CTA's second pipeline fill is never issued
+        lib.fp8_gemm_dense(qa_d, sa_d, qb_d, sb_d)
+        with pytest.raises(lib.Fp8fgError) as ei:
+            lib.check()
+        assert ei.value.code == lib.ERR_TIMEOUT
+    finally:
+        lib.debug_set(2, -1)
+        lib.debug_set(1, 0)
+    c = lib.fp8_gemm_dense(qa_d, sa_d, qb_d, sb_d)
+    lib.check()
+    compare_gemm(c, gemm.gemm_dense(qa, sa, qb, sb), True)
+
+
 # ---------------------------------------------------------------- split-K (decode-sized M)
 def _split_case(fg, M, N, K, seed, out_dtype=torch.bfloat16, accumulate=False):
     x = wl.activations(M, K, seed, device="cpu")
