@@ -53,16 +53,31 @@ namespace {
 
 using namespace gemm_detail;
 
+#ifndef FP8FG_PAIR_GROUPS
+#define FP8FG_PAIR_GROUPS 2
+#endif
+#ifndef FP8FG_PAIR_ISSUERS
+#define FP8FG_PAIR_ISSUERS FP8FG_PAIR_GROUPS
+#endif
+
 struct PairCfg {
   static constexpr int kStages = 5;
   static constexpr int kTileM = 2 * BM;   // rows of a pair tile
   static constexpr int kTileN = 256;      // columns of a pair tile
-  static constexpr int kHalfCols = 128;   // TMEM columns of one half buffer (MMA N)
-  static constexpr int kHalfBufs = 4;
+  // MMA groups per K block: 2 = two N=128 groups into 128-column buffers
+  // (four in TMEM), 1 = one N=256 group into 256-column buffers (two)
+  static constexpr int kGroups = FP8FG_PAIR_GROUPS;
+  static constexpr int kHalfCols = kTileN / kGroups;  // TMEM columns of one buffer (MMA N)
+  static constexpr int kHalfBufs = 512 / kHalfCols;
+  static constexpr int kGroupRows = (kTileN / 2) / kGroups;  // B rows of each CTA per group
   static constexpr int kTmemCols = 512;
+  // MMA-issuing threads (leader, lane 0 of warps 1 .. kIssuers): issuer i
+  // takes the groups h with h % kIssuers == i, so that the instruction
+  // stream of a K block is split over SM sub-partitions
+  static constexpr int kIssuers = FP8FG_PAIR_ISSUERS;
   static constexpr int kEpiWarps = 8;
-  static constexpr int kEpiWarp0 = 2;
-  static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;  // 320: 204 registers a thread
+  static constexpr int kEpiWarp0 = kIssuers > 1 ? 4 : 2;
+  static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;  // 168 registers a thread either way
   static constexpr int kNC = 128;                                 // accumulator columns per thread
   static constexpr int kABytes = BM * BK;                         // this CTA's 128 rows of A
   static constexpr int kBBytes = (kTileN / 2) * BK;               // this CTA's half of B
@@ -81,7 +96,7 @@ struct PairCfg {
   static constexpr int kOffBar = kOffSbw + kEpiWarps * kSbwChunk * 4;
   // full[S] (leader: A and B of both CTAs), sfull[S] (scales), empty[S],
   // tfull[4], tempty[4] (leader: 2 x 8 promotion warps), drain
-  static constexpr int kNumBars = 3 * kStages + 2 * kHalfBufs + 1;
+  static constexpr int kNumBars = 3 * kStages + 2 * kHalfBufs + kIssuers;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kSmem = kOffTmemSlot + 16 + 1024;
   static_assert(kHalfBufs * kHalfCols == kTmemCols, "half buffers fill TMEM");
@@ -118,7 +133,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
   auto empty_bar = [bar0](uint32_t s) { return bar0 + (2 * S + s) * 8; };
   auto tfull_bar = [bar0](uint32_t b) { return bar0 + (3 * S + b) * 8; };
   auto tempty_bar = [bar0](uint32_t b) { return bar0 + (3 * S + NB + b) * 8; };
-  const uint32_t drain_bar = bar0 + (3 * S + 2 * NB) * 8;
+  auto drain_bar = [bar0](uint32_t i) { return bar0 + (3 * S + 2 * NB + i) * 8; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmemSlot);
 
   if (warp == 0 && lane == 0) {
@@ -135,10 +150,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
       mbar_init(tfull_bar(b), 1);
       mbar_init(tempty_bar(b), 2 * C::kEpiWarps);
     }
-    mbar_init(drain_bar, 1);
+    for (int i = 0; i < C::kIssuers; ++i) mbar_init(drain_bar(i), 1);
     fence_barrier_init();
   }
-  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);  // both CTAs
   tc_fence_before();
   // both CTAs' barriers exist and TMEM is allocated before any cross-CTA
   // arrival, TMA completion or MMA
@@ -163,7 +178,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
         const int nb0 = n0 + static_cast<int>(rank) * (C::kTileN / 2);
         for (int kb = 0; kb < a.KB; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1;
-          if (!mbar_wait(empty_bar(s), ph ^ 1, a.status, kStatusTimeoutProducer, a.wait_limit_ns)) {
+          if (!role_wait(empty_bar(s), ph ^ 1, a.status, kStatusTimeoutProducer, a.wait_limit_ns)) {
             ok = false;
             break;
           }
@@ -185,31 +200,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
         if (leader) mbar_wait(full_bar(i % S), (i / S) & 1, nullptr, 0, a.wait_limit_ns);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (leader)
-    if (leader && lane == 0) {
+  } else if (warp < C::kEpiWarp0) {
+    // ------------------------------------------------------------ MMA issuers (leader)
+    const int issuer = warp - 1;
+    if (leader && lane == 0 && issuer < C::kIssuers) {
       constexpr uint32_t idesc = f8_idesc(C::kTileM, C::kHalfCols);
       uint32_t it = 0;
       bool ok = true;
       for (int t = pair; ok && t < a.num_tiles; t += npairs) {
         for (int kb = 0; kb < a.KB && ok; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1;
-          if (!mbar_wait(full_bar(s), ph, a.status, kStatusTimeoutMma, a.wait_limit_ns)) {
+          if (!role_wait(full_bar(s), ph, a.status, kStatusTimeoutMma, a.wait_limit_ns)) {
             ok = false;
             break;
           }
           const uint64_t ad = kmajor_sw128_desc(sbase + C::kOffA + s * C::kABytes);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t u = 2 * it + h;
+          for (int h = issuer; h < C::kGroups; h += C::kIssuers) {
+            const uint32_t u = C::kGroups * it + h;
             const uint32_t b = u % NB, tph = (u / NB) & 1;
-            if (!mbar_wait(tempty_bar(b), tph ^ 1, a.status, kStatusTimeoutMma, a.wait_limit_ns)) {
+            if (!role_wait(tempty_bar(b), tph ^ 1, a.status, kStatusTimeoutMma, a.wait_limit_ns)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            // rows 64h .. 64h+63 of each CTA's B half: 8 swizzle atoms of 1 KB
-            const uint64_t bd = kmajor_sw128_desc(sbase + C::kOffB + s * C::kBBytes + h * 64 * BK);
+            // the group's rows of each CTA's B half (whole 1 KB swizzle atoms)
+            const uint64_t bd = kmajor_sw128_desc(sbase + C::kOffB + s * C::kBBytes + h * C::kGroupRows * BK);
             const uint32_t d = tmem_base + b * C::kHalfCols;
 #pragma unroll
             for (int k = 0; k < BK / 32; ++k) mma_f8f6f4_pair(d, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
@@ -217,9 +233,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
           }
         }
       }
-      // All MMAs complete before TMEM is released.
-      mma_commit_pair(drain_bar, 0x1);
-      if (!mbar_wait(drain_bar, 0, nullptr, 0, a.wait_limit_ns)) atomicCAS(a.status, 0u, kStatusTimeoutDrain);
+      // All MMAs of this issuer complete before TMEM is released.
+      mma_commit_pair(drain_bar(issuer), 0x1);
+      if (!mbar_wait(drain_bar(issuer), 0, nullptr, 0, a.wait_limit_ns)) atomicCAS(a.status, 0u, kStatusTimeoutDrain);
     }
   } else {
     // ------------------------------------------------------------ promotion + epilogue
@@ -273,8 +289,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
         if constexpr (!kBRow) sc = sa * sbw[jb % C::kSbwChunk];
         const float* sbv = smem_sb + s * C::kTileN + col0;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t u = 2 * it + h;
+        for (int h = 0; h < C::kGroups; ++h) {
+          const uint32_t u = C::kGroups * it + h;
           const uint32_t b = u % NB, tph = (u / NB) & 1;
           const bool got = mbar_wait(tfull_bar(b), tph, a.status, kStatusTimeoutEpilogue, a.wait_limit_ns);
           if (!__all_sync(0xffffffffu, got)) {
@@ -282,12 +298,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
             break;
           }
           tc_fence_after();
-          const uint32_t taddr = tmem_base + lane_bits + b * C::kHalfCols + g * 64;
+          const uint32_t taddr = tmem_base + lane_bits + b * C::kHalfCols + g * C::kGroupRows;
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
+          for (int ch = 0; ch < C::kGroupRows / 16; ++ch) {
             uint32_t r[16];
             tmem_ld16(taddr + ch * 16, r);
-            promote<16, kBRow>(acc + h * 64 + ch * 16, r, sc, sa, sbv + h * 64 + ch * 16);
+            promote<16, kBRow>(acc + h * C::kGroupRows + ch * 16, r, sc, sa, sbv + h * C::kGroupRows + ch * 16);
           }
           tc_fence_before();
           __syncwarp();
