@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         if (ti.skip) continue;
         for (int kb = ti.kb0; kb < ti.kb0 + ti.kbc; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1;
-          if (!role_wait(empty_bar(s), ph ^ 1, a.status, kStatusTimeoutProducer, a.wait_limit_ns)) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1, a.status, kStatusTimeoutProducer, a.wait_limit_ns)) {
             ok = false;
             break;
           }
@@ -383,8 +383,8 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         for (int kb = ti.kb0; kb < ti.kb0 + ti.kbc; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1;
           const uint32_t buf = it % NB, tph = (it / NB) & 1;
-          if (!role_wait(tempty_bar(buf), tph ^ 1, a.status, kStatusTimeoutMma, a.wait_limit_ns) ||
-              !role_wait(full_bar(s), ph, a.status, kStatusTimeoutMma, a.wait_limit_ns)) {
+          if (!mbar_wait(tempty_bar(buf), tph ^ 1, a.status, kStatusTimeoutMma, a.wait_limit_ns) ||
+              !mbar_wait(full_bar(s), ph, a.status, kStatusTimeoutMma, a.wait_limit_ns)) {
             ok = false;
             break;
           }

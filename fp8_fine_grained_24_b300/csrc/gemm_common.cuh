@@ -178,18 +178,6 @@ __device__ __forceinline__ void promote(float* acc, const uint32_t (&r)[W], floa
   }
 }
 
-// Bounded wait of the single-thread roles (TMA producer, MMA issuer), which
-// share an SM sub-partition with promotion warps. With FP8FG_ROLE_SLEEP the
-// polls sleep (try_wait with a suspend-time hint) instead of spinning.
-__device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, uint32_t* status, uint32_t code,
-                                          uint64_t limit_ns) {
-#ifdef FP8FG_ROLE_SLEEP
-  return mbar_wait_sleep(bar, parity, status, code, limit_ns);
-#else
-  return mbar_wait(bar, parity, status, code, limit_ns);
-#endif
-}
-
 // ---------------------------------------------------------------- host side
 inline int64_t ld4(int64_t r) { return (r + 3) / 4 * 4; }
 

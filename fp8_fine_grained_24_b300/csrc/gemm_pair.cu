@@ -8,35 +8,33 @@
 //
 // Why pairs. One CTA computing a 128 x 256 tile reads its A and B operands
 // from shared memory for every MMA and has TMA write them there: for every
-// 128-K block about 96 KB pass through that SM's shared memory, close to its
-// bandwidth at the tensor core's rate. With cta_group::2 the two CTAs of a
-// cluster compute one 256 x 256 tile: each loads its own 128 rows of A and
-// half of the tile's B (128 rows), and the tensor cores of the pair share
-// the B halves, so every SM moves 64 KB per K block. The other gain is
-// deeper accumulator buffering: the pair issues the tile's K block as two
-// MMA groups of N = 128 (one per 64-row slice of each B half), each into its
-// own 128-column TMEM buffer. Four such buffers fill the 512 columns, so the
-// tensor core can run one and a half K blocks ahead of the promotion warps
-// (against one K block with two 256-column buffers).
+// 128-K block about 96 KB pass through that SM's shared memory. With
+// cta_group::2 the two CTAs of a cluster compute one 256 x 256 tile: each
+// loads its own 128 rows of A and half of the tile's B (128 rows), and the
+// tensor cores of the pair share the B halves, so every SM moves 64 KB per
+// K block. Measured on B300 (4096 x N x 7168, BF16 out): level with the
+// single-CTA kernel under sustained, power-capped load (+2.5% at N=24576,
+// where the lower operand traffic lets the clock sit higher), 2-4% behind
+// it in short bursts. So it is an option (fp8fg_debug_set key 3), not the
+// default.
 //
 // Roles (each CTA, 10 warps):
 //   warp 0     TMA producer: this CTA's A rows and B half into a 5-stage
 //              ring. A and B completions count on the LEADER's full barrier
 //              (both CTAs' bytes); the scales land on a local barrier.
-//   warp 1     leader only: MMA issuer. Per K block and half h: wait for the
-//              half buffer to be released by the promotion warps of both
-//              CTAs, issue 4 x tcgen05.mma.cta_group::2 (M 256, N 128, K 32),
-//              commit to the buffer's "full" barrier in both CTAs.
+//   warp 1     leader only: MMA issuer. Per K block: wait for an
+//              accumulator buffer released by the promotion warps of both
+//              CTAs, issue 4 x tcgen05.mma.cta_group::2 (M 256, N 256,
+//              K 32), commit to the buffer's "full" barrier in both CTAs.
 //   warps 2-9  promotion + epilogue. Warp w reads TMEM lanes 32*(w%4)...
-//              (its rows) and columns 64*g.. of each half buffer, g = the
-//              warp's column group: over the two halves that is tile columns
-//              128*g .. 128*g+127, inside one 128x128 block of B scales.
-//              acc += (sA * sB) * partial per K block, then the tile is
-//              stored through shared-memory staging and TMA stores.
-// TMEM column c of half buffer h holds tile column 64*h + c for c < 64 (B
-// rows from the leader's half) and 128 + 64*h + (c - 64) for c >= 64 (the
-// peer's half): the MMA takes the first N/2 B rows from the leader's shared
-// memory and the rest from the peer's.
+//              (its rows) and the 128 columns of its column group g: tile
+//              columns 128*g .. 128*g+127, inside one 128x128 block of B
+//              scales. acc += (sA * sB) * partial per K block, then the tile
+//              is stored through shared-memory staging and TMA stores.
+// TMEM column c of a buffer holds tile column c: the MMA takes B rows
+// 0..N/2-1 from the leader's shared memory and the rest from the peer's.
+// (With two groups, column c of group h's buffer holds tile column
+// 64*h + c for c < 64 and 128 + 64*h + (c - 64) otherwise.)
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
@@ -53,28 +51,24 @@ namespace {
 
 using namespace gemm_detail;
 
-#ifndef FP8FG_PAIR_GROUPS
-#define FP8FG_PAIR_GROUPS 2
-#endif
-#ifndef FP8FG_PAIR_ISSUERS
-#define FP8FG_PAIR_ISSUERS FP8FG_PAIR_GROUPS
-#endif
-
 struct PairCfg {
   static constexpr int kStages = 5;
   static constexpr int kTileM = 2 * BM;   // rows of a pair tile
   static constexpr int kTileN = 256;      // columns of a pair tile
-  // MMA groups per K block: 2 = two N=128 groups into 128-column buffers
-  // (four in TMEM), 1 = one N=256 group into 256-column buffers (two)
-  static constexpr int kGroups = FP8FG_PAIR_GROUPS;
+  // MMA groups per K block: 1 = one N=256 group into a 256-column buffer
+  // (two in TMEM); 2 = two N=128 groups into 128-column buffers (four).
+  // Two groups halve the MMA work per instruction, and one issuing thread
+  // (about 30-50 ns per tcgen05.mma next to busy promotion warps) then
+  // bounds the K block: measured 20-25% slower than one group, and still
+  // 10% slower with the groups split over two issuing threads.
+  static constexpr int kGroups = 1;
   static constexpr int kHalfCols = kTileN / kGroups;  // TMEM columns of one buffer (MMA N)
   static constexpr int kHalfBufs = 512 / kHalfCols;
   static constexpr int kGroupRows = (kTileN / 2) / kGroups;  // B rows of each CTA per group
   static constexpr int kTmemCols = 512;
   // MMA-issuing threads (leader, lane 0 of warps 1 .. kIssuers): issuer i
-  // takes the groups h with h % kIssuers == i, so that the instruction
-  // stream of a K block is split over SM sub-partitions
-  static constexpr int kIssuers = FP8FG_PAIR_ISSUERS;
+  // takes the groups h with h % kIssuers == i
+  static constexpr int kIssuers = 1;
   static constexpr int kEpiWarps = 8;
   static constexpr int kEpiWarp0 = kIssuers > 1 ? 4 : 2;
   static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;  // 168 registers a thread either way
@@ -178,7 +172,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
         const int nb0 = n0 + static_cast<int>(rank) * (C::kTileN / 2);
         for (int kb = 0; kb < a.KB; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1;
-          if (!role_wait(empty_bar(s), ph ^ 1, a.status, kStatusTimeoutProducer, a.wait_limit_ns)) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1, a.status, kStatusTimeoutProducer, a.wait_limit_ns)) {
             ok = false;
             break;
           }
@@ -210,7 +204,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
       for (int t = pair; ok && t < a.num_tiles; t += npairs) {
         for (int kb = 0; kb < a.KB && ok; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1;
-          if (!role_wait(full_bar(s), ph, a.status, kStatusTimeoutMma, a.wait_limit_ns)) {
+          if (!mbar_wait(full_bar(s), ph, a.status, kStatusTimeoutMma, a.wait_limit_ns)) {
             ok = false;
             break;
           }
@@ -219,7 +213,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
           for (int h = issuer; h < C::kGroups; h += C::kIssuers) {
             const uint32_t u = C::kGroups * it + h;
             const uint32_t b = u % NB, tph = (u / NB) & 1;
-            if (!role_wait(tempty_bar(b), tph ^ 1, a.status, kStatusTimeoutMma, a.wait_limit_ns)) {
+            if (!mbar_wait(tempty_bar(b), tph ^ 1, a.status, kStatusTimeoutMma, a.wait_limit_ns)) {
               ok = false;
               break;
             }
@@ -413,11 +407,11 @@ cudaError_t pair_setup(int* max_pairs) {
 }  // namespace
 
 namespace {
-// FP8FG_PAIR=0 in the environment, or fp8fg_debug_set(3, 0), keeps every
-// problem on the single-CTA kernel (A/B comparisons of the two kernels).
+// Off by default; FP8FG_PAIR=1 in the environment, or fp8fg_debug_set(3, 1),
+// sends large dense problems to the pair kernel.
 std::atomic<int> g_pair_enabled{[] {
   const char* v = std::getenv("FP8FG_PAIR");
-  return (v && v[0] == '0') ? 0 : 1;
+  return (v && v[0] == '1') ? 1 : 0;
 }()};
 }  // namespace
 

@@ -75,9 +75,9 @@ void gemm_workspace_zero_range(int mode, int64_t rows, int64_t N, int64_t K, int
 cudaError_t launch_gemm(const GemmProblem& p, uint32_t* status, uint64_t wait_limit_ns, int debug_skip_fill,
                         int num_sms, cudaStream_t stream, const char** detail);
 
-// The CTA-pair GEMM (gemm_pair.cu): taken for dense problems large enough to
-// fill the GPU with 256 x 256 tiles (pair_gemm_eligible); launch_gemm
-// dispatches to it.
+// The CTA-pair GEMM (gemm_pair.cu): when switched on, taken for dense
+// problems large enough to fill the GPU with 256 x 256 tiles
+// (pair_gemm_eligible); launch_gemm dispatches to it.
 bool pair_gemm_eligible(const GemmProblem& p, int num_sms);
 void set_pair_gemm_enabled(bool on);
 cudaError_t launch_gemm_pair(const GemmProblem& p, uint32_t* status, uint64_t wait_limit_ns, int debug_skip_fill,

@@ -285,10 +285,10 @@ FP8FG_API int fp8fg_study_mma_accumulation(const uint8_t* A, const uint8_t* B, f
  *          of its k-th pipeline fill (value k >= 0; -1 disables), so that
  *          the consumers' bounded waits run out and the call reports
  *          FP8FG_ERR_TIMEOUT without faulting;
- *   key 3: 1 (default) lets large dense GEMMs run on CTA pairs (tcgen05
- *          cta_group::2, 256 x 256 tiles); 0 keeps every GEMM on the
- *          single-CTA kernel (the environment variable FP8FG_PAIR=0 sets
- *          the same at load time).
+ *   key 3: 1 sends large dense GEMMs (more 128x256 tiles than half the
+ *          SMs) to the CTA-pair kernel (tcgen05 cta_group::2, 256 x 256
+ *          tiles); 0 (the default) keeps every GEMM on the single-CTA
+ *          kernel. The environment variable FP8FG_PAIR=1 sets 1 at load.
  * Returns FP8FG_OK or FP8FG_ERR_INVALID_ARG.
  */
 FP8FG_API int fp8fg_debug_set(int key, int64_t value);

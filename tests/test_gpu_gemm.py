@@ -100,15 +100,19 @@ def test_dense_outputs_stay_in_bounds(lib):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("N", wl.PREFILL_NS)
-def test_dense_prefill_sampled(lib, N):
+@pytest.mark.parametrize("N,pair", [(n, 0) for n in wl.PREFILL_NS] + [(7168, 1)])
+def test_dense_prefill_sampled(lib, N, pair):
     M, K = wl.PREFILL_M, wl.PREFILL_K
     x = wl.activations(M, K, 1001, device="cuda")
     w = wl.weights((N, K), 2000 + N, device="cuda")
     qa_d, sa_d = lib.fp8_quant_1x128(x)
     qb_d, sb_d = lib.fp8_quant_128x128(w)
-    c = lib.fp8_gemm_dense(qa_d, sa_d, qb_d, sb_d)
-    torch.cuda.synchronize()
+    try:
+        lib.debug_set(3, pair)   # 1: the CTA-pair kernel
+        c = lib.fp8_gemm_dense(qa_d, sa_d, qb_d, sb_d)
+        torch.cuda.synchronize()
+    finally:
+        lib.debug_set(3, 0)
     rng = np.random.default_rng(N)
     rows = np.unique(np.concatenate([[0, M - 1], rng.choice(M, 62, replace=False)]))
     nblocks = np.unique(np.concatenate([[0, (N - 1) // 128], rng.choice((N + 127) // 128, 2, replace=False)]))
@@ -385,9 +389,9 @@ def test_timeout_reports_error_and_context_survives(lib):
 
 
 # ---------------------------------------------------------------- CTA pairs (large dense problems)
-# Dense problems whose 128 x 256 tiles outnumber half the SMs run on CTA
-# pairs (tcgen05 cta_group::2, 256 x 256 tiles). Debug key 3 switches the
-# pair kernel off, so both kernels can be checked on the same shapes.
+# Debug key 3 sends dense problems whose 128 x 256 tiles outnumber half the
+# SMs to the CTA-pair kernel (tcgen05 cta_group::2, 256 x 256 tiles); it is
+# off by default. Both kernels are checked on the same shapes.
 PAIR_SHAPES = [
     (1000, 2600, 1024, torch.bfloat16),   # ragged: the last pair tile's peer rows and B half partly out of range
     (2048, 2560, 2048, torch.float32),
@@ -403,7 +407,7 @@ def test_pair_and_single_cta_kernels_match_oracle(lib, M, N, K, out_dtype, pair)
         lib.debug_set(3, pair)
         _dense_case(lib, M, N, K, seed=M + N + K, out_dtype=out_dtype)
     finally:
-        lib.debug_set(3, 1)
+        lib.debug_set(3, 0)
 
 
 def test_pair_kernel_row_scaled_accumulate(lib):
@@ -412,9 +416,13 @@ def test_pair_kernel_row_scaled_accumulate(lib):
     qgT, sgT, qxT, sxT = _wgrad_operands(T, N, C, 87)
     base = wl.normal((N, C), 88, device="cuda")
     out = base.clone()
-    lib.fp8_gemm_dense_out(dev(qgT), dev(pad_rows_scale(sgT, N)), dev(qxT), dev(pad_rows_scale(sxT, C)), out,
-                           b_scale_kind=lib.SCALE_ROW, accumulate=True)
-    lib.check()
+    try:
+        lib.debug_set(3, 1)
+        lib.fp8_gemm_dense_out(dev(qgT), dev(pad_rows_scale(sgT, N)), dev(qxT), dev(pad_rows_scale(sxT, C)), out,
+                               b_scale_kind=lib.SCALE_ROW, accumulate=True)
+        lib.check()
+    finally:
+        lib.debug_set(3, 0)
     compare_gemm(out, gemm.wgrad(qgT, sgT, qxT, sxT) + base.double().cpu().numpy(), False)
 
 
@@ -426,17 +434,21 @@ def test_pair_kernel_timeout_reports_error_and_context_survives(lib):
     qb, sb, qb_d, sb_d = _quant_b(w)
     lib.check()
     try:
+        lib.debug_set(3, 1)
         lib.debug_set(1, 50_000_000)   # 50 ms wait limit
         lib.debug_set(2, 1)            # every CTA's second pipeline fill is never issued
         lib.fp8_gemm_dense(qa_d, sa_d, qb_d, sb_d)
         with pytest.raises(lib.Fp8fgError) as ei:
             lib.check()
         assert ei.value.code == lib.ERR_TIMEOUT
+        lib.debug_set(2, -1)
+        lib.debug_set(1, 0)
+        c = lib.fp8_gemm_dense(qa_d, sa_d, qb_d, sb_d)
+        lib.check()
     finally:
         lib.debug_set(2, -1)
         lib.debug_set(1, 0)
-    c = lib.fp8_gemm_dense(qa_d, sa_d, qb_d, sb_d)
-    lib.check()
+        lib.debug_set(3, 0)
     compare_gemm(c, gemm.gemm_dense(qa, sa, qb, sb), True)
 
 
