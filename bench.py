@@ -493,7 +493,8 @@ def run_e2e(step, fg, torch, device, steps, barrier):
 # experts and 8192 Zipf-routed tokens, (N, K) in {(4096, 7168), (7168,
 # 2048)}; grouped-masked MoE, 16 experts of <= 256 tokens, N=4096, K=7168;
 # its weight gradient; the 128x1 requantization from E4M3 and from BF16;
-# and the small dense case.
+# the small dense case; and the prefill GEMM with its output quantized in
+# the epilogue, beside the unfused GEMM + quantizer pair.
 CONFIG_CASES = (
     ("gemm", (128, 256, 512), None),
     ("gemm", (64, 7168, 16384), None),
@@ -506,6 +507,8 @@ CONFIG_CASES = (
     ("wgrad", (16, 256, 4096, 7168), None),
     ("requant", (4096, 7168), "e4m3"),
     ("requant", (4096, 7168), "bf16"),
+    ("gemm_quant", (4096, 7168, 7168), None),
+    ("gemm_then_quant", (4096, 7168, 7168), None),
 )
 
 
@@ -621,6 +624,8 @@ def time_case(case, dims, src="e4m3", steps=20, warmup=5, graph_reps=10, rotate=
     """Time one kernel on one shape through a captured CUDA graph; returns a dict.
 
     gemm M,N,K        dense GEMM, bf16 out (operands quantized once, untimed)
+    gemm_quant M,N,K  dense GEMM whose output is quantized per 1x128 tile in the epilogue
+    gemm_then_quant M,N,K  the unfused pair: dense GEMM (bf16 out), then fp8_quant_1x128
     contig E,T,N,K    grouped-contiguous MoE GEMM: T tokens routed by Zipf(1.1) counts
     masked E,M,N,K    grouped-masked MoE GEMM: uniform counts up to M tokens per expert
     wgrad E,T,N,C     masked-K weight gradient dW_e = G_e^T X_e (128x1 pow2 operands, FP32 out)
@@ -645,6 +650,31 @@ def time_case(case, dims, src="e4m3", steps=20, warmup=5, graph_reps=10, rotate=
             ws = None if (not workspace) else fg.gemm_workspace(M, N, K, device=dev)
             return (lambda: fg.fp8_gemm_dense_out(qa, sa, qb, sb, c, workspace=ws),
                     gemm_bytes(M, N, K), gemm_flops(M, N, K))
+        if case == "gemm_quant":
+            # the GEMM with its output quantized per 1x128 tile in the epilogue
+            M, N, K = dims
+            qa, sa = fg.fp8_quant_1x128(wl.activations(M, K, seed, device=dev))
+            qb, sb = fg.fp8_quant_128x128(wl.weights((N, K), seed + 1, device=dev))
+            q = torch.empty((M, N), dtype=torch.uint8, device=dev)
+            s = torch.empty((N // 128, fg.scale_ld(M)), dtype=torch.float32, device=dev)
+            ws = None if (not workspace) else fg.gemm_workspace(M, N, K, device=dev)
+            nb = M * K + N * K + M * (K // 128) * 4 + (N // 128) * (K // 128) * 4 + M * N + M * (N // 128) * 4
+            return (lambda: fg.fp8_gemm_dense_quant_out(qa, sa, qb, sb, q, s, workspace=ws), nb, gemm_flops(M, N, K))
+        if case == "gemm_then_quant":
+            # the unfused pair: BF16 GEMM, then fp8_quant_1x128 of its output
+            M, N, K = dims
+            qa, sa = fg.fp8_quant_1x128(wl.activations(M, K, seed, device=dev))
+            qb, sb = fg.fp8_quant_128x128(wl.weights((N, K), seed + 1, device=dev))
+            c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            q = torch.empty((M, N), dtype=torch.uint8, device=dev)
+            s = torch.empty((N // 128, fg.scale_ld(M)), dtype=torch.float32, device=dev)
+            ws = None if (not workspace) else fg.gemm_workspace(M, N, K, device=dev)
+
+            def both():
+                fg.fp8_gemm_dense_out(qa, sa, qb, sb, c, workspace=ws)
+                fg.fp8_quant_1x128_out(c, q, s)
+            nb = M * K + N * K + M * (K // 128) * 4 + (N // 128) * (K // 128) * 4 + M * N + M * (N // 128) * 4
+            return both, nb, gemm_flops(M, N, K)
         if case == "contig":
             E, T, N, K = dims
             counts = wl.zipf_counts(T, E, 1.1, seed)
@@ -782,7 +812,8 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--src", choices=["e4m3", "bf16", "fp32"], default="e4m3",
                     help="requant case: source type (E4M3 with 1x128 scales, BF16 or FP32)")
-    ap.add_argument("--case", choices=["gemm", "contig", "masked", "wgrad", "quant1x128", "quant128x128", "requant"],
+    ap.add_argument("--case", choices=["gemm", "gemm_quant", "gemm_then_quant", "contig", "masked", "wgrad",
+                                       "quant1x128", "quant128x128", "requant"],
                     default=None,
                     help="time a single kernel on --shape instead of the full step")
     ap.add_argument("--shape", default="4096,7168,7168")

@@ -79,6 +79,8 @@ _SIGS = {
     "fp8_gemm_dense": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_int, _c_int, _c_i64, _c_i64, _c_i64,
                                 _c_vp, _c_sz, _c_vp]),
     "fp8fg_gemm_workspace_size": (_c_sz, [_c_i64, _c_i64, _c_i64]),
+    "fp8_gemm_dense_quant": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_vp, _c_vp, _c_int, _c_i64, _c_i64,
+                                      _c_i64, _c_vp, _c_sz, _c_vp]),
     "fp8_gemm_grouped_contig": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_i64, _c_i64, _c_i64,
                                          _c_i64, _c_vp]),
     "fp8_gemm_grouped_masked": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_int, _c_vp, _c_int, _c_int,
@@ -235,6 +237,30 @@ def fp8_gemm_dense(a, sa, b, sb, out_dtype=torch.bfloat16, b_scale_kind=SCALE_BL
     return fp8_gemm_dense_out(a, sa, b, sb, c, b_scale_kind, False, ws, stream)
 
 
+def fp8_gemm_dense_quant_out(a, sa, b, sb, q, s, c=None, pow2=False, workspace=None, stream=None):
+    """Dense GEMM whose BF16 result is quantized per 1x128 tile in the epilogue:
+    q [M, N] uint8 E4M3, s [N/128, ld(M)] fp32; c (BF16 [M, N]) optional."""
+    M, K = a.shape
+    N = b.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.fp8_gemm_dense_quant(_ptr(_as_u8(a)), _ptr(sa), _ptr(_as_u8(b)), _ptr(sb), SCALE_BLOCK128, _ptr(q),
+                                    _ptr(s), _ptr(c), int(bool(pow2)), M, N, K, _ptr(workspace), ws_bytes,
+                                    _stream(stream)))
+    return q, s
+
+
+def fp8_gemm_dense_quant(a, sa, b, sb, pow2=False, with_bf16=False, stream=None):
+    """(q, s) or (q, s, c): the GEMM's result quantized per 1x128 tile (and its BF16 form)."""
+    M, K = a.shape
+    N = b.shape[0]
+    q = torch.empty((M, N), dtype=torch.uint8, device=a.device)
+    s = torch.empty((N // 128, scale_ld(M)), dtype=torch.float32, device=a.device)
+    c = torch.empty((M, N), dtype=torch.bfloat16, device=a.device) if with_bf16 else None
+    ws = gemm_workspace(M, N, K, device=a.device)
+    fp8_gemm_dense_quant_out(a, sa, b, sb, q, s, c, pow2, ws, stream)
+    return (q, s, c) if with_bf16 else (q, s)
+
+
 def fp8_gemm_grouped_contig_out(a, sa, b, sb, m_indices, c, stream=None):
     M_total, K = a.shape
     E, N, _ = b.shape
@@ -283,6 +309,7 @@ __all__ = [
     "lib", "LIB_PATH", "Fp8fgError", "scale_ld", "version", "check", "debug_set",
     "fp8_quant_1x128", "fp8_quant_1x128_out", "fp8_quant_128x128", "fp8_quant_128x128_out",
     "fp8_requant_128x1", "fp8_requant_128x1_out", "gemm_workspace_size", "gemm_workspace",
-    "fp8_gemm_dense", "fp8_gemm_dense_out", "fp8_gemm_grouped_contig", "fp8_gemm_grouped_contig_out",
+    "fp8_gemm_dense", "fp8_gemm_dense_out", "fp8_gemm_dense_quant", "fp8_gemm_dense_quant_out",
+    "fp8_gemm_grouped_contig", "fp8_gemm_grouped_contig_out",
     "fp8_gemm_grouped_masked", "fp8_gemm_grouped_masked_out", "study_mma_accumulation",
 ]

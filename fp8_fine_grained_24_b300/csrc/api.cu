@@ -239,6 +239,35 @@ int fp8_gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const fl
   return run_gemm(p, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int fp8_gemm_dense_quant(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, int b_scale_kind,
+                         uint8_t* q, float* s, void* C, int pow2, int64_t M, int64_t N, int64_t K, void* workspace,
+                         size_t workspace_bytes, fp8fg_stream_t stream) {
+  if (M == 0 || N == 0) {
+    if (M < 0 || N < 0 || K < 0) return fail(FP8FG_ERR_INVALID_ARG, "negative size");
+    return FP8FG_OK;
+  }
+  if (pow2 != 0 && pow2 != 1) return fail(FP8FG_ERR_INVALID_ARG, "pow2 must be 0 or 1");
+  if (!q || !s) return fail(FP8FG_ERR_INVALID_ARG, "null pointer");
+  // the common checks, with q standing in for C when no BF16 C is wanted
+  int rc = check_gemm_common(A, sA, B, sB, b_scale_kind, C ? C : static_cast<void*>(q), FP8FG_BF16, 0, M, N, K);
+  if (rc) return rc;
+  if (b_scale_kind != FP8FG_SCALE_BLOCK128)
+    return fail(FP8FG_ERR_INVALID_ARG, "fused quantization takes 128x128 block-scaled B");
+  if (N % 128 != 0) return fail(FP8FG_ERR_UNSUPPORTED_SHAPE, "N=%lld must be a multiple of 128", (long long)N);
+  if (!aligned16(q) || !aligned16(s)) return fail(FP8FG_ERR_MISALIGNED, "q and s must be 16-byte aligned");
+  fp8fg::GemmProblem p{};
+  p.mode = fp8fg::kModeDense;
+  p.A = A; p.sA = sA; p.B = B; p.sB = sB; p.b_row = 0;
+  p.C = C; p.out_f32 = 0; p.accumulate = 0;
+  p.rows = M; p.N = N; p.K = K; p.groups = 1; p.groupsB = 1;
+  p.q_out = q; p.s_out = s; p.pow2_out = pow2;
+  if (workspace != nullptr && !aligned16(workspace))
+    return fail(FP8FG_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+  p.workspace = workspace;
+  p.workspace_bytes = workspace ? workspace_bytes : 0;
+  return run_gemm(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int fp8_gemm_grouped_contig(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
                             const int32_t* m_indices, void* C, int out_dtype, int64_t M_total, int64_t N, int64_t K,
                             int64_t E, fp8fg_stream_t stream) {

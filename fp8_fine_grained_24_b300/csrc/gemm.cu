@@ -34,6 +34,7 @@
 
 #include "common.cuh"
 #include "gemm_common.cuh"
+#include "quant_math.cuh"
 #include "kernels.h"
 #include "launch.h"
 #include "tmap.h"
@@ -285,11 +286,65 @@ __device__ __forceinline__ bool sk_reduce(const KArgs& a, const Tile& ti, int ro
   return true;
 }
 
-template <int BN, bool kBRow, bool kF32, bool kSplit, bool kCompact>
+// Fused 1x128 quantization of one epilogue warp's 32 rows x 128 columns of
+// C (DeepSeek-V3 report excerpt, page 1, paragraph 3: activations are
+// quantized per 1x128 tile; the DeepGEMM article's call to fuse the FP8 cast
+// into the data movement, page 2, last paragraph). Every thread owns one
+// row's 128 columns, one whole tile: the value quantized is C rounded to
+// BF16 (what the unfused path writes and fp8_quant_1x128 then reads), the
+// scale fl32(amax / 448) (or its power of two), the code E4M3(RN(x / s)) by
+// the quantizer's own arithmetic, so the result is bit-identical to
+// fp8_gemm_dense followed by fp8_quant_1x128. Codes go out through the
+// warp's staging area (eight 16-byte chunks a row, 128-byte swizzle) and one
+// TMA store; scales are stored directly, 32 consecutive floats a warp.
+__device__ __forceinline__ void quant_store_tile(const KArgs& a, const Tile& ti, int row_in_tile, int col0, int lane,
+                                                 uint8_t* region, const CUtensorMap* tmQ, float (&acc)[128]) {
+  // BF16 rounding, packed in place (acc[i] <- the pair of columns 2i, 2i+1)
+  float am = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    const uint32_t w = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+    am = fmaxf(am, fmaxf(fabsf(__uint_as_float(w << 16)), fabsf(__uint_as_float(w & 0xFFFF0000u))));
+    acc[i] = __uint_as_float(w);
+  }
+  const float s = tile_scale(am, a.pow2_out != 0);
+  const float r = __frcp_rn(s);
+  const int path = warp_quot_mode(make_tile_div_mode(s));
+  // the staging area is free once earlier stores from it have read it
+  if (lane == 0) bulk_wait_read_all();
+  fence_async_shared();
+  __syncwarp();
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint64_t v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = neg_bf16x2(__float_as_uint(acc[c * 8 + i]));
+    quot2_n<8>(v, path, s, r);
+    uint4 o;
+    o.x = e4m3x4_pk(v[0], v[1]);
+    o.y = e4m3x4_pk(v[2], v[3]);
+    o.z = e4m3x4_pk(v[4], v[5]);
+    o.w = e4m3x4_pk(v[6], v[7]);
+    *reinterpret_cast<uint4*>(region + lane * 128 + ((c ^ (lane & 7)) << 4)) = o;
+  }
+  fence_async_shared();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_3d(tmQ, smem_u32(region), ti.n0 + col0, ti.m0 + (row_in_tile & ~31), 0);
+    bulk_commit();
+  }
+  const int row = ti.m0 + row_in_tile;
+  if (row < a.rows) a.s_out[static_cast<int64_t>((ti.n0 + col0) / 128) * a.ld_s + row] = s;
+}
+
+template <int BN, bool kBRow, bool kF32, bool kSplit, bool kCompact, bool kQ>
 __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
-                    const __grid_constant__ CUtensorMap tmC, const KArgs a) {
+                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmQ,
+                    const KArgs a) {
+  static_assert(!kQ || (BN == 256 && !kBRow && !kF32 && !kCompact),
+                "fused quantization: 128-column warps of BF16 output, dense layout");
   using C = Cfg<BN>;
   constexpr int S = C::kStages;
   constexpr int NB = C::kAccBufs;
@@ -511,7 +566,15 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
             region = smem + C::kOffB + held * C::kBBytes + (ew - 2) * C::kEpiWarpBytes;
           else if (ew >= C::kBorrowWarps)
             region = smem + C::kOffEpi + (ew - C::kBorrowWarps) * C::kEpiWarpBytes;
-          if (region != nullptr) staged = store_tile_tma<NC, kF32>(a, ti, row_in_tile, col0, lane, region, &tmC, acc);
+          if constexpr (kQ) {
+            // BF16 C (if asked for), then its 1x128 quantization through the
+            // same staging area
+            if (a.c_bf16) staged = store_tile_tma<NC, false>(a, ti, row_in_tile, col0, lane, region, &tmC, acc);
+            quant_store_tile(a, ti, row_in_tile, col0, lane, region, &tmQ, acc);
+            staged = true;
+          } else {
+            if (region != nullptr) staged = store_tile_tma<NC, kF32>(a, ti, row_in_tile, col0, lane, region, &tmC, acc);
+          }
         }
         if (!staged) store_row<NC, kF32>(a, ti, row_in_tile, col0, acc);
       }
@@ -541,7 +604,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
 
 // Raise the kernel's dynamic shared-memory limit once per device (the call
 // costs tens of microseconds of host time, so it is not repeated per launch).
-template <int BN, bool kBRow, bool kF32, bool kSplit, bool kCompact>
+template <int BN, bool kBRow, bool kF32, bool kSplit, bool kCompact, bool kQ = false>
 cudaError_t ensure_smem_attr() {
   static std::atomic<uint64_t> done{0};
   int dev = 0;
@@ -555,12 +618,12 @@ cudaError_t ensure_smem_attr() {
     // raised counts, forever if it never can: refuse to launch a build whose
     // register count does not cover the split.
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, fp8_gemm_kernel<BN, kBRow, kF32, kSplit, kCompact>);
+    e = cudaFuncGetAttributes(&fa, fp8_gemm_kernel<BN, kBRow, kF32, kSplit, kCompact, kQ>);
     if (e != cudaSuccess) return e;
     if (static_cast<long>(fa.numRegs) * C::kThreads < 128L * C::kRegsLow + 256L * C::kRegsHigh)
       return cudaErrorInvalidConfiguration;
   }
-  e = cudaFuncSetAttribute(fp8_gemm_kernel<BN, kBRow, kF32, kSplit, kCompact>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(fp8_gemm_kernel<BN, kBRow, kF32, kSplit, kCompact, kQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg<BN>::kSmem);
   if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
   return e;
@@ -582,6 +645,15 @@ struct Plan {
 };
 
 constexpr int64_t kMinUnits = 4;
+
+// Workspace layout: arrival counters first, in a region of fixed size (16
+// per split tile, at most num_sms / 2 split tiles), then the partial tiles.
+// The counter region only ever holds counters, which every call returns to
+// zero, so calls whose plans differ (tile width, shape) can share one
+// workspace: none of them finds another's partial sums where it counts.
+size_t counter_region_bytes(int num_sms) {
+  return (static_cast<size_t>(num_sms / 2) * 16 * sizeof(int) + 255) / 256 * 256;
+}
 
 int64_t gcd64(int64_t x, int64_t y) {
   while (y != 0) {
@@ -611,8 +683,8 @@ Plan plan_gemm(int mode, int64_t rows, int64_t N, int64_t K, int64_t groups, int
   const int64_t lcm = KB / gcd64(KB, per) * per;
   const int64_t segs = 1 + (units - 1) / KB + (units - 1) / per - (units - 1) / lcm;
   const size_t partial = static_cast<size_t>(segs) * BM * bn * sizeof(float);
-  const size_t counts = static_cast<size_t>(tiles - dp) * 16 * sizeof(int);
-  if (partial + counts > ws_avail) return p;
+  const size_t counts = counter_region_bytes(num_sms);
+  if (static_cast<size_t>(tiles - dp) * 16 * sizeof(int) > counts || partial + counts > ws_avail) return p;
   p.sk = true;
   p.grid = static_cast<int>((units + per - 1) / per);
   p.dp_tiles = static_cast<int>(dp);
@@ -642,13 +714,19 @@ bool encode_maps(const GemmProblem& p, MapSet* m) {
     m->sb = m->sa;  // unused
   }
   const int64_t groupsC = groupsA;
-  if (C::kTmaStore) {
+  if (C::kTmaStore && p.C != nullptr) {
     const int64_t esz = p.out_f32 ? 4 : 2;
     ok = ok && make_map(&m->c, p.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.C,
                         p.N, p.rows, groupsC, p.N * esz, p.rows * p.N * esz, 128 / esz, 32,
                         CU_TENSOR_MAP_SWIZZLE_128B);
   } else {
     m->c = m->sa;  // unused
+  }
+  if (p.q_out != nullptr) {
+    ok = ok && make_map(&m->q, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.q_out, p.N, p.rows, 1, p.N, p.rows * p.N, 128, 32,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    m->q = m->sa;  // unused
   }
   return ok;
 }
@@ -658,7 +736,7 @@ bool get_maps(const GemmProblem& p, MapSet* out) {
   MapKey k;
   std::memset(&k, 0, sizeof(k));  // padding bytes take part in the comparison
   const int64_t groupsA = (p.mode == kModeMaskedRows || p.mode == kModeMaskedK) ? p.groups : 1;
-  k.A = p.A; k.B = p.B; k.sA = p.sA; k.sB = p.b_row ? p.sB : nullptr; k.C = p.C;
+  k.A = p.A; k.B = p.B; k.sA = p.sA; k.sB = p.b_row ? p.sB : nullptr; k.C = p.C; k.Q = p.q_out;
   k.rows = p.rows; k.N = p.N; k.K = p.K; k.groupsA = groupsA; k.groupsB = p.groupsB; k.groupsC = groupsA;
   k.kind = BN; k.b_row = p.b_row; k.out_f32 = p.out_f32;
   if (map_cache_find(k, out)) return true;
@@ -682,6 +760,7 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
   const CUtensorMap& tmSA = ms.sa;
   const CUtensorMap& tmSB = ms.sb;
   const CUtensorMap& tmC = ms.c;
+  const CUtensorMap& tmQ = ms.q;
   KArgs a;
   a.mode = p.mode;
   a.KB = static_cast<int>(KB);
@@ -714,22 +793,26 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
   a.sk_units = a.sk_per_cta = a.sk_lcm = 0;
   a.ws_partial = nullptr;
   a.ws_count = nullptr;
+  a.s_out = p.s_out;
+  a.ld_s = ld4(p.rows);
+  a.pow2_out = p.pow2_out;
+  a.c_bf16 = p.C != nullptr;
   if (a.num_tiles == 0) return cudaSuccess;
   const Plan plan = plan_gemm(p.mode, p.rows, p.N, p.K, p.groups, num_sms, BN,
                               p.workspace != nullptr ? p.workspace_bytes : 0);
 
-  using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, KArgs);
+  using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, KArgs);
   // whole tiles / Stream-K / active tiles of the masked-rows layout
   KernelFn kernels[3] = {nullptr, nullptr, nullptr};
   const bool masked = p.mode == kModeMaskedRows;
   cudaError_t e = cudaSuccess;
-  const int variant = (p.b_row ? 4 : 0) + (p.out_f32 ? 2 : 0);
+  const int variant = p.q_out != nullptr ? 8 : (p.b_row ? 4 : 0) + (p.out_f32 ? 2 : 0);
   switch (variant) {
 #define FP8FG_VARIANT(V, R, F)                                                   \
   case V:                                                                        \
-    kernels[0] = fp8_gemm_kernel<BN, R, F, false, false>;                        \
-    kernels[1] = fp8_gemm_kernel<BN, R, F, true, false>;                         \
-    kernels[2] = fp8_gemm_kernel<BN, R, F, false, true>;                         \
+    kernels[0] = fp8_gemm_kernel<BN, R, F, false, false, false>;                 \
+    kernels[1] = fp8_gemm_kernel<BN, R, F, true, false, false>;                  \
+    kernels[2] = fp8_gemm_kernel<BN, R, F, false, true, false>;                  \
     e = masked ? ensure_smem_attr<BN, R, F, false, true>()                       \
                : ensure_smem_attr<BN, R, F, false, false>();                     \
     if (e == cudaSuccess && plan.sk) e = ensure_smem_attr<BN, R, F, true, false>(); \
@@ -739,22 +822,35 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
     FP8FG_VARIANT(4, true, false)
     FP8FG_VARIANT(6, true, true)
 #undef FP8FG_VARIANT
+    default:
+      // fused 1x128 quantization of the BF16 output (dense, 128x256 tiles)
+      if constexpr (BN == 256) {
+        kernels[0] = fp8_gemm_kernel<BN, false, false, false, false, true>;
+        kernels[1] = fp8_gemm_kernel<BN, false, false, true, false, true>;
+        e = ensure_smem_attr<BN, false, false, false, false, true>();
+        if (e == cudaSuccess && plan.sk) e = ensure_smem_attr<BN, false, false, true, false, true>();
+      } else {
+        e = cudaErrorInvalidValue;
+      }
+      break;
   }
   if (e != cudaSuccess) {
     *detail = "cudaFuncSetAttribute(max dynamic shared memory) failed";
     return e;
   }
   if (!plan.sk) {
-    e = launch_kernel(kernels[masked ? 2 : 0], dim3(plan.grid), dim3(C::kThreads), C::kSmem, stream, tmA, tmB, tmSA, tmSB, tmC, a);
+    e = launch_kernel(kernels[masked ? 2 : 0], dim3(plan.grid), dim3(C::kThreads), C::kSmem, stream, tmA, tmB, tmSA,
+                      tmSB, tmC, tmQ, a);
   } else {
     a.dp_tiles = plan.dp_tiles;
     a.sk_tile0 = plan.dp_tiles;
     a.sk_units = static_cast<int>(plan.sk_units);
     a.sk_per_cta = static_cast<int>(plan.sk_per_cta);
     a.sk_lcm = static_cast<int>(plan.sk_lcm);
-    a.ws_partial = static_cast<float*>(p.workspace);
-    a.ws_count = reinterpret_cast<int*>(static_cast<char*>(p.workspace) + plan.partial_bytes);
-    e = launch_kernel(kernels[1], dim3(plan.grid), dim3(C::kThreads), C::kSmem, stream, tmA, tmB, tmSA, tmSB, tmC, a);
+    a.ws_count = static_cast<int*>(p.workspace);
+    a.ws_partial = reinterpret_cast<float*>(static_cast<char*>(p.workspace) + plan.count_bytes);
+    e = launch_kernel(kernels[1], dim3(plan.grid), dim3(C::kThreads), C::kSmem, stream, tmA, tmB, tmSA, tmSB, tmC, tmQ,
+                      a);
   }
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) *detail = "GEMM kernel launch failed";
@@ -766,7 +862,8 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
 // Stream-K to spread the weight stream over, measured 25.2 -> 19.6 us at
 // 128x4096x7168 and 37.4 -> 30.8 us at 64x7168x16384. 256 for the rest,
 // where it is the fastest at every prefill and MoE shape measured.
-int pick_bn(int mode, int64_t rows) {
+int pick_bn(int mode, int64_t rows, bool quant_out = false) {
+  if (quant_out) return 256;  // the fused quantization needs 128-column warps
   static int forced = [] {
     const char* v = std::getenv("FP8FG_BN");
     if (!v) return 0;
@@ -822,21 +919,27 @@ void map_cache_put(const MapKey& k, const MapSet& m) {
 }  // namespace gemm_detail
 
 size_t gemm_workspace_bytes(int mode, int64_t rows, int64_t N, int64_t K, int64_t groups, int num_sms) {
-  const Plan plan = plan_gemm(mode, rows, N, K, groups, num_sms, pick_bn(mode, rows), SIZE_MAX);
-  return plan.sk ? plan.partial_bytes + plan.count_bytes : 0;
+  // enough for the plain and the fused-quantization tile choice of the shape
+  size_t need = 0;
+  for (bool q : {false, true}) {
+    const Plan plan = plan_gemm(mode, rows, N, K, groups, num_sms, pick_bn(mode, rows, q), SIZE_MAX);
+    if (plan.sk && plan.partial_bytes + plan.count_bytes > need) need = plan.partial_bytes + plan.count_bytes;
+  }
+  return need;
 }
 
 void gemm_workspace_zero_range(int mode, int64_t rows, int64_t N, int64_t K, int64_t groups, int num_sms,
                                size_t workspace_bytes, size_t* offset, size_t* bytes) {
   const Plan plan = plan_gemm(mode, rows, N, K, groups, num_sms, pick_bn(mode, rows), workspace_bytes);
-  *offset = plan.sk ? plan.partial_bytes : 0;
+  *offset = 0;
   *bytes = plan.sk ? plan.count_bytes : 0;
 }
 
 cudaError_t launch_gemm(const GemmProblem& p, uint32_t* status, uint64_t wait_limit_ns, int debug_skip_fill,
                         int num_sms, cudaStream_t stream, const char** detail) {
-  if (pair_gemm_eligible(p, num_sms)) return launch_gemm_pair(p, status, wait_limit_ns, debug_skip_fill, stream, detail);
-  switch (pick_bn(p.mode, p.rows)) {
+  if (p.q_out == nullptr && pair_gemm_eligible(p, num_sms))
+    return launch_gemm_pair(p, status, wait_limit_ns, debug_skip_fill, stream, detail);
+  switch (pick_bn(p.mode, p.rows, p.q_out != nullptr)) {
     case 192: return launch_bn<192>(p, status, wait_limit_ns, debug_skip_fill, num_sms, stream, detail);
     case 256: return launch_bn<256>(p, status, wait_limit_ns, debug_skip_fill, num_sms, stream, detail);
     default: return launch_bn<128>(p, status, wait_limit_ns, debug_skip_fill, num_sms, stream, detail);

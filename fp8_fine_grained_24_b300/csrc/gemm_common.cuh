@@ -44,6 +44,11 @@ struct KArgs {
   int sk_units, sk_per_cta, sk_lcm;  // the planner keeps them below 2^31
   float* ws_partial;
   int* ws_count;
+  // fused 1x128 quantization of the BF16 output (the kQ kernel variant)
+  float* s_out;
+  int64_t ld_s;
+  int pow2_out;
+  int c_bf16;  // the BF16 C is stored as well
 };
 
 struct Tile {
@@ -191,12 +196,13 @@ struct MapKey {
   const void* sA;
   const void* sB;
   const void* C;
+  const void* Q;
   int64_t rows, N, K, groupsA, groupsB, groupsC;
   int32_t kind, b_row, out_f32, pad;  // kind: tile configuration of the launch
 };
 
 struct MapSet {
-  CUtensorMap a, b, sa, sb, c;
+  CUtensorMap a, b, sa, sb, c, q;
 };
 
 // Thread-safe lookup / insertion (gemm.cu); a lookup that misses returns false.

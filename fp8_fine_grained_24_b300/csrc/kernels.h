@@ -49,6 +49,12 @@ struct GemmProblem {
   const int32_t* masked;
   void* workspace;          // Stream-K scratch (zeroed before first use), or nullptr
   size_t workspace_bytes;
+  // Fused quantization of the output (dense only; C, if not null, is BF16):
+  // the BF16-rounded C quantized per 1x128 tile to E4M3 codes q_out [rows][N]
+  // and scales s_out [N/128][ld(rows)]. q_out == nullptr: no quantization.
+  uint8_t* q_out;
+  float* s_out;
+  int pow2_out;
 };
 
 // Bytes of Stream-K workspace launch_gemm uses for this problem when given

@@ -164,6 +164,30 @@ FP8FG_API int fp8_gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B
                    void* workspace, size_t workspace_bytes, fp8fg_stream_t stream);
 
 /*
+ * fp8_gemm_dense_quant -- fp8_gemm_dense with the FP8 cast of its output
+ * fused in: the result, rounded to BF16, is quantized per 1x128 tile for the
+ * next layer's GEMM in the GEMM's own epilogue, instead of being written in
+ * BF16 and read back by fp8_quant_1x128. (DeepSeek-V3 report excerpt,
+ * page 1, paragraph 3: activations quantized per 1x128 tile; page 2, last
+ * paragraph: the request to fuse the FP8 cast with the data movement.)
+ * Bit-identical to fp8_gemm_dense (BF16 out) followed by fp8_quant_1x128 of
+ * its output.
+ *
+ *   A, sA, B, sB  as fp8_gemm_dense, b_scale_kind FP8FG_SCALE_BLOCK128
+ *   q          [M][N] E4M3 codes of the BF16 result, written
+ *   s          [N/128][ld(M)] float scales, written (the sA layout the next
+ *              GEMM takes)
+ *   C          NULL, or [M][N] BF16: the unquantized result as well
+ *   pow2       0: s = amax/448; 1: power-of-2 scales
+ *   workspace  as fp8_gemm_dense (fp8fg_gemm_workspace_size covers both)
+ * Requires K % 128 == 0, N % 128 == 0, 16-byte aligned A, B, q, s (and C).
+ */
+FP8FG_API int fp8_gemm_dense_quant(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                                   int b_scale_kind, uint8_t* q, float* s, void* C, int pow2,
+                                   int64_t M, int64_t N, int64_t K,
+                                   void* workspace, size_t workspace_bytes, fp8fg_stream_t stream);
+
+/*
  * fp8_gemm_dense_noalloc -- fp8_gemm_dense for callers that cannot allocate
  * device memory. (No counterpart in the paper: a deployment convenience of
  * this library.) Some callers only receive device pointers from a host
@@ -189,9 +213,9 @@ FP8FG_API int fp8_gemm_dense_noalloc(const uint8_t* A, const float* sA, const ui
                                      int b_scale_kind, void* C, int out_dtype, int accumulate,
                                      int64_t M, int64_t N, int64_t K, fp8fg_stream_t stream);
 
-/* Bytes of workspace fp8_gemm_dense uses for this shape on the current
- * device (0 if it does not split tiles along K). Needs a CUDA device; 0 on
- * error. */
+/* Bytes of workspace fp8_gemm_dense and fp8_gemm_dense_quant use for this
+ * shape on the current device (0 if neither splits tiles along K); one
+ * workspace of this size serves both. Needs a CUDA device; 0 on error. */
 FP8FG_API size_t fp8fg_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /*
