@@ -26,6 +26,8 @@ Layouts:
 * Wgrad:              dW[N,C] = sum_t G[t,n] X[t,c]; with both operands
   128x1-requantized and transposed it is the dense form with per-row scales
   on both sides.
+* Dgrad:              dX[M,K] = dY[M,N] W[N,K], W the forward pass's
+  128x128-quantized weight read as it is (no transposed copy).
 """
 from __future__ import annotations
 
@@ -116,6 +118,23 @@ def wgrad(qgT, sgT, qxT, sxT, rows=None, cols=None) -> np.ndarray:
     qgT [N, T] with sgT [T/128, N]; qxT [C, T] with sxT [T/128, C].
     """
     return gemm_dense(qgT, sgT, qxT, sxT, "row", rows=rows, cols=cols)
+
+
+def dgrad(qdy, sdy, qw, sw, rows=None, cols=None) -> np.ndarray:
+    """dX[M, K] = dYhat @ What: the data gradient of Y = X W^T.
+
+    qdy [M, N] with 1x128 scales sdy [N/128, M] (quantized along N, the
+    reduction); qw [N, K] with its 128x128 block scales sw [N/128, K/128],
+    the forward pass's quantized weight, used as is (DeepSeek-V3 report
+    excerpt, page 1, paragraph 3: Dgrad is one of the FP8 GEMMs).
+    """
+    a = dequant_rows(np.asarray(qdy), sdy)
+    b = dequant_blocks(np.asarray(qw), sw)
+    if rows is not None:
+        a = a[np.asarray(rows)]
+    if cols is not None:
+        b = b[:, np.asarray(cols)]
+    return a @ b
 
 
 def frobenius_rel(c, ref) -> float:

@@ -162,3 +162,54 @@ def test_tolerance_helpers():
     assert ok.tolist() == [True, True, True, True]
     ok = gemm.elementwise_ok(ref + np.array([0.1, 0.0, 0.0, 0.0]), ref)
     assert ok.tolist() == [False, True, True, True]
+
+
+# ---------------------------------------------------------------- Dgrad
+def test_dgrad_matches_exact_rationals():
+    # dX[m, k] = sum_n dYhat[m, n] What[n, k] with W's block scales indexed
+    # [n // 128, k // 128] (the forward weight read as it is)
+    rng = np.random.default_rng(31)
+    M, N, K = 4, 384, 260
+    qdy = _codes(rng, (M, N))
+    qw = _codes(rng, (N, K))
+    sdy = _rand_scales(rng, (N // 128, M))
+    sw = _rand_scales(rng, (N // 128, 3))
+    dx = gemm.dgrad(qdy, sdy, qw, sw)
+    for m, k in [(0, 0), (3, 259), (1, 130), (2, 127), (0, 128)]:
+        ex = Fraction(0)
+        for n in range(N):
+            a = Fraction(float(e4m3.decode(qdy[m, n]))) * Fraction(float(sdy[n // 128, m]))
+            b = Fraction(float(e4m3.decode(qw[n, k]))) * Fraction(float(sw[n // 128, k // 128]))
+            ex += a * b
+        assert abs(Fraction(dx[m, k]) - ex) <= abs(ex) * Fraction(1, 2 ** 45) + Fraction(1, 2 ** 80)
+
+
+def test_block_quantization_is_transpose_invariant_and_dgrad_is_dense_on_wt():
+    # A 128x128 block has one amax whichever way it is read, so quantizing
+    # W^T gives the transposed codes and scales; dgrad on W then equals the
+    # dense product with B = W^T quantized on its own.
+    rng = np.random.default_rng(32)
+    N, K, M = 256, 384, 6
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    qw, sw = quant.quant_128x128(w)
+    qwT, swT = quant.quant_128x128(np.ascontiguousarray(w.T))
+    assert np.array_equal(qwT, qw.T) and np.array_equal(swT, sw.T)
+    dy = rng.standard_normal((M, N)).astype(np.float32)
+    qdy, sdy = quant.quant_1x128(dy)
+    np.testing.assert_allclose(gemm.dgrad(qdy, sdy, qw, sw), gemm.gemm_dense(qdy, sdy, qwT, swT), rtol=1e-12,
+                               atol=1e-12)
+
+
+def test_dgrad_block_scale_indexing_with_distinct_powers():
+    # unit codes everywhere and a distinct power of two per weight block:
+    # dX[m, k] = 128 * sum_j sw[j, k // 128], which a transposed or shifted
+    # scale index would change
+    N, K, M = 384, 256, 2
+    one = e4m3.encode(np.ones(1))[0]
+    qdy = np.full((M, N), one, np.uint8)
+    qw = np.full((N, K), one, np.uint8)
+    sdy = np.ones((N // 128, M), np.float32)
+    sw = np.exp2(np.arange(6).reshape(3, 2) * 3).astype(np.float32)   # [N/128, K/128]
+    dx = gemm.dgrad(qdy, sdy, qw, sw)
+    for k in (0, 127, 128, 255):
+        assert dx[0, k] == 128.0 * sw[:, k // 128].sum()
