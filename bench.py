@@ -493,8 +493,9 @@ def run_e2e(step, fg, torch, device, steps, barrier):
 # experts and 8192 Zipf-routed tokens, (N, K) in {(4096, 7168), (7168,
 # 2048)}; grouped-masked MoE, 16 experts of <= 256 tokens, N=4096, K=7168;
 # its weight gradient; the 128x1 requantization from E4M3 and from BF16;
-# the small dense case; and the prefill GEMM with its output quantized in
-# the epilogue, beside the unfused GEMM + quantizer pair.
+# the small dense case; the prefill GEMM with its output quantized in the
+# epilogue, beside the unfused GEMM + quantizer pair; the data gradient of
+# the N=7168 prefill layer; and the dense weight gradient over 4096 tokens.
 CONFIG_CASES = (
     ("gemm", (128, 256, 512), None),
     ("gemm", (64, 7168, 16384), None),
@@ -509,6 +510,8 @@ CONFIG_CASES = (
     ("requant", (4096, 7168), "bf16"),
     ("gemm_quant", (4096, 7168, 7168), None),
     ("gemm_then_quant", (4096, 7168, 7168), None),
+    ("dgrad", (4096, 7168, 7168), None),
+    ("wgrad_dense", (4096, 4096, 7168), None),
 )
 
 
@@ -626,6 +629,8 @@ def time_case(case, dims, src="e4m3", steps=20, warmup=5, graph_reps=10, rotate=
     gemm M,N,K        dense GEMM, bf16 out (operands quantized once, untimed)
     gemm_quant M,N,K  dense GEMM whose output is quantized per 1x128 tile in the epilogue
     gemm_then_quant M,N,K  the unfused pair: dense GEMM (bf16 out), then fp8_quant_1x128
+    dgrad M,N,K       data gradient dX[M,K] = dY[M,N] W[N,K] (W read MN-major), bf16 out
+    wgrad_dense T,N,C dense weight gradient dW[N,C] += G^T X over T tokens (128x1 pow2, FP32 accumulate)
     contig E,T,N,K    grouped-contiguous MoE GEMM: T tokens routed by Zipf(1.1) counts
     masked E,M,N,K    grouped-masked MoE GEMM: uniform counts up to M tokens per expert
     wgrad E,T,N,C     masked-K weight gradient dW_e = G_e^T X_e (128x1 pow2 operands, FP32 out)
@@ -675,6 +680,26 @@ def time_case(case, dims, src="e4m3", steps=20, warmup=5, graph_reps=10, rotate=
                 fg.fp8_quant_1x128_out(c, q, s)
             nb = M * K + N * K + M * (K // 128) * 4 + (N // 128) * (K // 128) * 4 + M * N + M * (N // 128) * 4
             return both, nb, gemm_flops(M, N, K)
+        if case == "dgrad":
+            # dX[M, K] = dY[M, N] W[N, K]: the forward weight read as its own transpose
+            M, N, K = dims
+            qdy, sdy = fg.fp8_quant_1x128(wl.normal((M, N), seed, device=dev, dtype=torch.bfloat16))
+            qw, sw = fg.fp8_quant_128x128(wl.weights((N, K), seed + 1, device=dev))
+            dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+            ws = None if (not workspace) else fg.gemm_workspace(M, K, N, device=dev)
+            return (lambda: fg.fp8_gemm_dgrad_out(qdy, sdy, qw, sw, dx, workspace=ws), gemm_bytes(M, K, N),
+                    gemm_flops(M, K, N))
+        if case == "wgrad_dense":
+            # dW[N, C] += G^T X over T tokens: both operands 128x1 (pow2), FP32 accumulate
+            T, N, C = dims
+            qgT, sgT = fg.fp8_requant_128x1(wl.normal((T, N), seed, device=dev, dtype=torch.bfloat16), pow2=True)
+            qx, sx = fg.fp8_quant_1x128(wl.activations(T, C, seed + 1, device=dev))
+            qxT, sxT = fg.fp8_requant_128x1(qx.view(torch.float8_e4m3fn), sx, pow2=True)
+            dw = torch.zeros((N, C), dtype=torch.float32, device=dev)
+            ws = None if (not workspace) else fg.gemm_workspace(N, C, T, device=dev)
+            nb = T * (N + C) + 2 * (T // 128) * (N + C) * 4 + 2 * N * C * 4   # dW read and written
+            return (lambda: fg.fp8_gemm_dense_out(qgT, sgT, qxT, sxT, dw, b_scale_kind=fg.SCALE_ROW, accumulate=True,
+                                                  workspace=ws), nb, 2.0 * T * N * C)
         if case == "contig":
             E, T, N, K = dims
             counts = wl.zipf_counts(T, E, 1.1, seed)
@@ -812,8 +837,8 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--src", choices=["e4m3", "bf16", "fp32"], default="e4m3",
                     help="requant case: source type (E4M3 with 1x128 scales, BF16 or FP32)")
-    ap.add_argument("--case", choices=["gemm", "gemm_quant", "gemm_then_quant", "contig", "masked", "wgrad",
-                                       "quant1x128", "quant128x128", "requant"],
+    ap.add_argument("--case", choices=["gemm", "gemm_quant", "gemm_then_quant", "dgrad", "wgrad_dense", "contig",
+                                       "masked", "wgrad", "quant1x128", "quant128x128", "requant"],
                     default=None,
                     help="time a single kernel on --shape instead of the full step")
     ap.add_argument("--shape", default="4096,7168,7168")

@@ -79,6 +79,8 @@ _SIGS = {
     "fp8_gemm_dense": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_int, _c_int, _c_i64, _c_i64, _c_i64,
                                 _c_vp, _c_sz, _c_vp]),
     "fp8fg_gemm_workspace_size": (_c_sz, [_c_i64, _c_i64, _c_i64]),
+    "fp8_gemm_dgrad": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_int, _c_i64, _c_i64, _c_i64, _c_vp,
+                                _c_sz, _c_vp]),
     "fp8_gemm_dense_quant": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_vp, _c_vp, _c_int, _c_i64, _c_i64,
                                       _c_i64, _c_vp, _c_sz, _c_vp]),
     "fp8_gemm_grouped_contig": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_int, _c_i64, _c_i64, _c_i64,
@@ -237,6 +239,25 @@ def fp8_gemm_dense(a, sa, b, sb, out_dtype=torch.bfloat16, b_scale_kind=SCALE_BL
     return fp8_gemm_dense_out(a, sa, b, sb, c, b_scale_kind, False, ws, stream)
 
 
+def fp8_gemm_dgrad_out(dy, s_dy, w, sw, dx, accumulate=False, workspace=None, stream=None):
+    """dX[M, K] (+)= dY[M, N] @ W[N, K] from dY's 1x128 and W's 128x128 quantization."""
+    M, N = dy.shape
+    K = w.shape[1]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.fp8_gemm_dgrad(_ptr(_as_u8(dy)), _ptr(s_dy), _ptr(_as_u8(w)), _ptr(sw), _ptr(dx), _dtype_code(dx),
+                              int(bool(accumulate)), M, N, K, _ptr(workspace), ws_bytes, _stream(stream)))
+    return dx
+
+
+def fp8_gemm_dgrad(dy, s_dy, w, sw, out_dtype=torch.bfloat16, stream=None):
+    """dX = dY @ W with W read as its own transpose (no transposed copy)."""
+    M = dy.shape[0]
+    N, K = w.shape
+    dx = torch.empty((M, K), dtype=out_dtype, device=dy.device)
+    ws = gemm_workspace(M, K, N, device=dy.device)
+    return fp8_gemm_dgrad_out(dy, s_dy, w, sw, dx, False, ws, stream)
+
+
 def fp8_gemm_dense_quant_out(a, sa, b, sb, q, s, c=None, pow2=False, workspace=None, stream=None):
     """Dense GEMM whose BF16 result is quantized per 1x128 tile in the epilogue:
     q [M, N] uint8 E4M3, s [N/128, ld(M)] fp32; c (BF16 [M, N]) optional."""
@@ -310,6 +331,7 @@ __all__ = [
     "fp8_quant_1x128", "fp8_quant_1x128_out", "fp8_quant_128x128", "fp8_quant_128x128_out",
     "fp8_requant_128x1", "fp8_requant_128x1_out", "gemm_workspace_size", "gemm_workspace",
     "fp8_gemm_dense", "fp8_gemm_dense_out", "fp8_gemm_dense_quant", "fp8_gemm_dense_quant_out",
+    "fp8_gemm_dgrad", "fp8_gemm_dgrad_out",
     "fp8_gemm_grouped_contig", "fp8_gemm_grouped_contig_out",
     "fp8_gemm_grouped_masked", "fp8_gemm_grouped_masked_out", "study_mma_accumulation",
 ]

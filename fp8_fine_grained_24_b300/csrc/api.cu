@@ -268,6 +268,29 @@ int fp8_gemm_dense_quant(const uint8_t* A, const float* sA, const uint8_t* B, co
   return run_gemm(p, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int fp8_gemm_dgrad(const uint8_t* dY, const float* s_dY, const uint8_t* W, const float* sW, void* dX, int out_dtype,
+                   int accumulate, int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+                   fp8fg_stream_t stream) {
+  if (M == 0 || K == 0) {
+    if (M < 0 || N < 0 || K < 0) return fail(FP8FG_ERR_INVALID_ARG, "negative size");
+    return FP8FG_OK;
+  }
+  // as a GEMM: rows M, output columns K, reduction N; B = W read MN-major
+  int rc = check_gemm_common(dY, s_dY, W, sW, FP8FG_SCALE_BLOCK128, dX, out_dtype, accumulate, M, K, N);
+  if (rc) return rc;
+  if (K % 16 != 0) return fail(FP8FG_ERR_UNSUPPORTED_SHAPE, "K=%lld must be a multiple of 16", (long long)K);
+  fp8fg::GemmProblem p{};
+  p.mode = fp8fg::kModeDense;
+  p.A = dY; p.sA = s_dY; p.B = W; p.sB = sW; p.b_row = 0; p.b_mn_major = 1;
+  p.C = dX; p.out_f32 = out_dtype == FP8FG_FP32; p.accumulate = accumulate;
+  p.rows = M; p.N = K; p.K = N; p.groups = 1; p.groupsB = 1;
+  if (workspace != nullptr && !aligned16(workspace))
+    return fail(FP8FG_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+  p.workspace = workspace;
+  p.workspace_bytes = workspace ? workspace_bytes : 0;
+  return run_gemm(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int fp8_gemm_grouped_contig(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
                             const int32_t* m_indices, void* C, int out_dtype, int64_t M_total, int64_t N, int64_t K,
                             int64_t E, fp8fg_stream_t stream) {

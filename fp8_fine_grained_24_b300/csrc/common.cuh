@@ -297,11 +297,28 @@ __device__ __forceinline__ uint64_t kmajor_sw128_desc(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand tile (the
+// non-reduction dimension contiguous) with the 128-byte swizzle: each
+// 128-byte row holds 128 consecutive MN elements of one K index, 8 rows (8
+// consecutive K) form a 1024-byte swizzle atom, atoms are packed along K
+// (stride 1024 B, bits 32-45), and the next 128 MN elements start
+// `mn_stride` bytes further (leading-byte offset, bits 16-29).
+__device__ __forceinline__ uint64_t mnmajor_sw128_desc(uint32_t smem_addr, uint32_t mn_stride) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
 // Instruction descriptor for kind::f8f6f4: D FP32 (bits 4-5 = 1), A and B
-// E4M3 (bits 7-9 and 10-12 = 0), both K-major (bits 15, 16 = 0),
-// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t f8_idesc(int m, int n) {
-  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+// E4M3 (bits 7-9 and 10-12 = 0), A K-major (bit 15 = 0), B K-major or, with
+// b_mn_major, MN-major (bit 16), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t f8_idesc(int m, int n, bool b_mn_major = false) {
+  return (1u << 4) | (b_mn_major ? (1u << 16) : 0u) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 // ---------------------------------------------------------------- clusters and CTA pairs

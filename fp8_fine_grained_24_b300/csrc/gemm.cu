@@ -333,18 +333,27 @@ __device__ __forceinline__ void quant_store_tile(const KArgs& a, const Tile& ti,
     tma_store_3d(tmQ, smem_u32(region), ti.n0 + col0, ti.m0 + (row_in_tile & ~31), 0);
     bulk_commit();
   }
+  // a warp whose 128 columns lie wholly past N (the last tile of an N that
+  // is not a multiple of 256) has no scale row to write
   const int row = ti.m0 + row_in_tile;
-  if (row < a.rows) a.s_out[static_cast<int64_t>((ti.n0 + col0) / 128) * a.ld_s + row] = s;
+  if (row < a.rows && ti.n0 + col0 < a.N) a.s_out[static_cast<int64_t>((ti.n0 + col0) / 128) * a.ld_s + row] = s;
 }
 
-template <int BN, bool kBRow, bool kF32, bool kSplit, bool kCompact, bool kQ>
+// Kernel variants besides the plain one: fused 1x128 quantization of the
+// output, or B read MN-major (the weight as its own transpose).
+enum : int { kVarPlain = 0, kVarQuant = 1, kVarBT = 2 };
+
+template <int BN, bool kBRow, bool kF32, bool kSplit, bool kCompact, int kVar>
 __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmQ,
                     const KArgs a) {
+  constexpr bool kQ = kVar == kVarQuant;
+  constexpr bool kBT = kVar == kVarBT;
   static_assert(!kQ || (BN == 256 && !kBRow && !kF32 && !kCompact),
                 "fused quantization: 128-column warps of BF16 output, dense layout");
+  static_assert(!kBT || (BN != 192 && !kBRow && !kCompact), "MN-major B: 128-column boxes, block scales");
   using C = Cfg<BN>;
   constexpr int S = C::kStages;
   constexpr int NB = C::kAccBufs;
@@ -412,7 +421,15 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
           mbar_arrive_expect_tx(full_bar(s), tx);
           if (static_cast<int>(it) == a.debug_skip_fill) continue;  // test hook: never filled
           tma_load_3d(sbase + C::kOffA + s * C::kABytes, &tmA, full_bar(s), kb * BK, ti.m0, ti.gA);
-          tma_load_3d(sbase + C::kOffB + s * C::kBBytes, &tmB, full_bar(s), kb * BK, ti.n0, ti.gB);
+          if constexpr (kBT) {
+            // [K][N] rows: boxes of 128 columns x 128 K, one per 128 columns
+#pragma unroll
+            for (int j = 0; j < BN / 128; ++j)
+              tma_load_3d(sbase + C::kOffB + s * C::kBBytes + j * 128 * BK, &tmB, full_bar(s), ti.n0 + j * 128,
+                          kb * BK, ti.gB);
+          } else {
+            tma_load_3d(sbase + C::kOffB + s * C::kBBytes, &tmB, full_bar(s), kb * BK, ti.n0, ti.gB);
+          }
           tma_load_3d(sbase + C::kOffSA + s * C::kSABytes, &tmSA, full_bar(s), ti.m0, kb, ti.gA);
           if (kBRow)
             tma_load_3d(sbase + C::kOffSB + s * C::kSBBytes, &tmSB, full_bar(s), ti.n0, kb, ti.gB);
@@ -428,7 +445,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
    } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = f8_idesc(BM, BN);
+      constexpr uint32_t idesc = f8_idesc(BM, BN, kBT);
       uint32_t it = 0;
       bool ok = true;
       Work wk = work_begin<kSplit>(a);
@@ -445,12 +462,16 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
           }
           tc_fence_after();
           const uint64_t ad = kmajor_sw128_desc(sbase + C::kOffA + s * C::kABytes);
-          const uint64_t bd = kmajor_sw128_desc(sbase + C::kOffB + s * C::kBBytes);
+          // K-major B advances 32 bytes along its rows per MMA; MN-major B
+          // 32 rows of 128 bytes (descriptor units of 16 bytes)
+          const uint64_t bd = kBT ? mnmajor_sw128_desc(sbase + C::kOffB + s * C::kBBytes, 128 * BK)
+                                  : kmajor_sw128_desc(sbase + C::kOffB + s * C::kBBytes);
+          constexpr uint64_t kBStep = kBT ? (32 * 128) >> 4 : 32 >> 4;
           const uint32_t d = tmem_base + buf * BN;
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k) {
             // advance 32 bytes (= 32 E4M3 elements) along K inside the swizzle atom
-            mma_f8f6f4(d, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
+            mma_f8f6f4(d, ad + 2 * k, bd + kBStep * k, idesc, k > 0 ? 1u : 0u);
           }
           mma_commit(tfull_bar(buf));
         }
@@ -496,12 +517,15 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         const uint32_t buf = it % NB, tph = (it / NB) & 1;
         if (!kBRow && (jb % C::kSbwChunk) == 0) {
           const int nbk = (ti.n0 + col0) / 128;
-          const float* src = a.sB + (static_cast<int64_t>(ti.gB) * a.sb_nblk + nbk) * a.sb_kblk + kb0;
+          const float* src = a.sB + static_cast<int64_t>(ti.gB) * a.sb_nblk * a.sb_kblk +
+                             static_cast<int64_t>(nbk) * a.sb_col_stride + static_cast<int64_t>(kb0) * a.sb_red_stride;
           __syncwarp();
 #pragma unroll
           for (int i = 0; i < C::kSbwChunk / 32; ++i) {
             const unsigned k = jb + i * 32 + lane;
-            sbw[i * 32 + lane] = (nbk < a.sb_nblk && k < static_cast<unsigned>(kbc)) ? __ldg(src + k) : 0.0f;
+            sbw[i * 32 + lane] =
+                (nbk < a.sb_nblk && k < static_cast<unsigned>(kbc)) ? __ldg(src + static_cast<int64_t>(k) * a.sb_red_stride)
+                                                                    : 0.0f;
           }
           __syncwarp();
         }
@@ -604,7 +628,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
 
 // Raise the kernel's dynamic shared-memory limit once per device (the call
 // costs tens of microseconds of host time, so it is not repeated per launch).
-template <int BN, bool kBRow, bool kF32, bool kSplit, bool kCompact, bool kQ = false>
+template <int BN, bool kBRow, bool kF32, bool kSplit, bool kCompact, int kVar = kVarPlain>
 cudaError_t ensure_smem_attr() {
   static std::atomic<uint64_t> done{0};
   int dev = 0;
@@ -618,12 +642,12 @@ cudaError_t ensure_smem_attr() {
     // raised counts, forever if it never can: refuse to launch a build whose
     // register count does not cover the split.
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, fp8_gemm_kernel<BN, kBRow, kF32, kSplit, kCompact, kQ>);
+    e = cudaFuncGetAttributes(&fa, fp8_gemm_kernel<BN, kBRow, kF32, kSplit, kCompact, kVar>);
     if (e != cudaSuccess) return e;
     if (static_cast<long>(fa.numRegs) * C::kThreads < 128L * C::kRegsLow + 256L * C::kRegsHigh)
       return cudaErrorInvalidConfiguration;
   }
-  e = cudaFuncSetAttribute(fp8_gemm_kernel<BN, kBRow, kF32, kSplit, kCompact, kQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(fp8_gemm_kernel<BN, kBRow, kF32, kSplit, kCompact, kVar>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg<BN>::kSmem);
   if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
   return e;
@@ -703,8 +727,12 @@ bool encode_maps(const GemmProblem& p, MapSet* m) {
   const int64_t groupsA = (p.mode == kModeMaskedRows || p.mode == kModeMaskedK) ? p.groups : 1;
   bool ok = make_map(&m->a, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.A, p.K, p.rows, groupsA, p.K, p.rows * p.K, BK, BM,
                      CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&m->b, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.B, p.K, p.N, p.groupsB, p.K, p.N * p.K, BK, BN,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
+  if (p.b_mn_major)  // B stored [K][N]: boxes of 128 columns x 128 K rows
+    ok = ok && make_map(&m->b, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.B, p.N, p.K, p.groupsB, p.N, p.N * p.K, 128, BK,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+  else
+    ok = ok && make_map(&m->b, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.B, p.K, p.N, p.groupsB, p.K, p.N * p.K, BK, BN,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && make_map(&m->sa, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.sA, p.rows, KB, groupsA, ld4(p.rows) * 4,
                       KB * ld4(p.rows) * 4, BM, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (p.b_row) {
@@ -738,7 +766,7 @@ bool get_maps(const GemmProblem& p, MapSet* out) {
   const int64_t groupsA = (p.mode == kModeMaskedRows || p.mode == kModeMaskedK) ? p.groups : 1;
   k.A = p.A; k.B = p.B; k.sA = p.sA; k.sB = p.b_row ? p.sB : nullptr; k.C = p.C; k.Q = p.q_out;
   k.rows = p.rows; k.N = p.N; k.K = p.K; k.groupsA = groupsA; k.groupsB = p.groupsB; k.groupsC = groupsA;
-  k.kind = BN; k.b_row = p.b_row; k.out_f32 = p.out_f32;
+  k.kind = p.b_mn_major ? -BN : BN; k.b_row = p.b_row; k.out_f32 = p.out_f32;
   if (map_cache_find(k, out)) return true;
   if (!encode_maps<BN>(p, out)) return false;
   map_cache_put(k, *out);
@@ -782,6 +810,8 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
   a.sB = p.sB;
   a.sb_nblk = static_cast<int>((p.N + 127) / 128);
   a.sb_kblk = static_cast<int>(KB);
+  a.sb_col_stride = p.b_mn_major ? 1 : a.sb_kblk;
+  a.sb_red_stride = p.b_mn_major ? a.sb_nblk : 1;
   a.C = p.C;
   a.ldc = p.N;
   a.c_group_stride = p.rows * p.N;
@@ -806,13 +836,14 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
   KernelFn kernels[3] = {nullptr, nullptr, nullptr};
   const bool masked = p.mode == kModeMaskedRows;
   cudaError_t e = cudaSuccess;
-  const int variant = p.q_out != nullptr ? 8 : (p.b_row ? 4 : 0) + (p.out_f32 ? 2 : 0);
+  const int variant = p.q_out != nullptr ? 8 : p.b_mn_major ? 10 + (p.out_f32 ? 1 : 0)
+                                                             : (p.b_row ? 4 : 0) + (p.out_f32 ? 2 : 0);
   switch (variant) {
 #define FP8FG_VARIANT(V, R, F)                                                   \
   case V:                                                                        \
-    kernels[0] = fp8_gemm_kernel<BN, R, F, false, false, false>;                 \
-    kernels[1] = fp8_gemm_kernel<BN, R, F, true, false, false>;                  \
-    kernels[2] = fp8_gemm_kernel<BN, R, F, false, true, false>;                  \
+    kernels[0] = fp8_gemm_kernel<BN, R, F, false, false, kVarPlain>;             \
+    kernels[1] = fp8_gemm_kernel<BN, R, F, true, false, kVarPlain>;              \
+    kernels[2] = fp8_gemm_kernel<BN, R, F, false, true, kVarPlain>;              \
     e = masked ? ensure_smem_attr<BN, R, F, false, true>()                       \
                : ensure_smem_attr<BN, R, F, false, false>();                     \
     if (e == cudaSuccess && plan.sk) e = ensure_smem_attr<BN, R, F, true, false>(); \
@@ -822,16 +853,34 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
     FP8FG_VARIANT(4, true, false)
     FP8FG_VARIANT(6, true, true)
 #undef FP8FG_VARIANT
-    default:
+    case 8:
       // fused 1x128 quantization of the BF16 output (dense, 128x256 tiles)
       if constexpr (BN == 256) {
-        kernels[0] = fp8_gemm_kernel<BN, false, false, false, false, true>;
-        kernels[1] = fp8_gemm_kernel<BN, false, false, true, false, true>;
-        e = ensure_smem_attr<BN, false, false, false, false, true>();
-        if (e == cudaSuccess && plan.sk) e = ensure_smem_attr<BN, false, false, true, false, true>();
+        kernels[0] = fp8_gemm_kernel<BN, false, false, false, false, kVarQuant>;
+        kernels[1] = fp8_gemm_kernel<BN, false, false, true, false, kVarQuant>;
+        e = ensure_smem_attr<BN, false, false, false, false, kVarQuant>();
+        if (e == cudaSuccess && plan.sk) e = ensure_smem_attr<BN, false, false, true, false, kVarQuant>();
       } else {
         e = cudaErrorInvalidValue;
       }
+      break;
+#define FP8FG_VARIANT_BT(V, F)                                                          \
+  case V:                                                                               \
+    if constexpr (BN != 192) {                                                          \
+      kernels[0] = fp8_gemm_kernel<BN, false, F, false, false, kVarBT>;                 \
+      kernels[1] = fp8_gemm_kernel<BN, false, F, true, false, kVarBT>;                  \
+      e = ensure_smem_attr<BN, false, F, false, false, kVarBT>();                       \
+      if (e == cudaSuccess && plan.sk) e = ensure_smem_attr<BN, false, F, true, false, kVarBT>(); \
+    } else {                                                                            \
+      e = cudaErrorInvalidValue;                                                        \
+    }                                                                                   \
+    break;
+    // B read MN-major (the data-gradient GEMM), BF16 or FP32 out
+    FP8FG_VARIANT_BT(10, false)
+    FP8FG_VARIANT_BT(11, true)
+#undef FP8FG_VARIANT_BT
+    default:
+      e = cudaErrorInvalidValue;
       break;
   }
   if (e != cudaSuccess) {
@@ -937,9 +986,11 @@ void gemm_workspace_zero_range(int mode, int64_t rows, int64_t N, int64_t K, int
 
 cudaError_t launch_gemm(const GemmProblem& p, uint32_t* status, uint64_t wait_limit_ns, int debug_skip_fill,
                         int num_sms, cudaStream_t stream, const char** detail) {
-  if (p.q_out == nullptr && pair_gemm_eligible(p, num_sms))
+  if (p.q_out == nullptr && !p.b_mn_major && pair_gemm_eligible(p, num_sms))
     return launch_gemm_pair(p, status, wait_limit_ns, debug_skip_fill, stream, detail);
-  switch (pick_bn(p.mode, p.rows, p.q_out != nullptr)) {
+  int bn = pick_bn(p.mode, p.rows, p.q_out != nullptr);
+  if (p.b_mn_major && bn == 192) bn = 256;
+  switch (bn) {
     case 192: return launch_bn<192>(p, status, wait_limit_ns, debug_skip_fill, num_sms, stream, detail);
     case 256: return launch_bn<256>(p, status, wait_limit_ns, debug_skip_fill, num_sms, stream, detail);
     default: return launch_bn<128>(p, status, wait_limit_ns, debug_skip_fill, num_sms, stream, detail);

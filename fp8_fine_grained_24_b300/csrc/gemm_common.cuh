@@ -26,6 +26,11 @@ struct KArgs {
   const int32_t* masked;
   const float* sB;
   int sb_nblk, sb_kblk;
+  // block scale of output-column block nb and K block kb of group g:
+  // sB[(g * sb_nblk * sb_kblk) + nb * sb_col_stride + kb * sb_red_stride]
+  // ([nb][kb] for weights quantized as B; [kb][nb], transposed, when the
+  // weight is read as its own transpose in the data-gradient GEMM)
+  int sb_col_stride, sb_red_stride;
   void* C;
   int64_t ldc;
   int64_t c_group_stride;

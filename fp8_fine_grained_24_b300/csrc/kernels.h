@@ -38,6 +38,7 @@ struct GemmProblem {
   const uint8_t* B;      // [groupsB][N][K]
   const float* sB;       // block: [groupsB][ceil(N/128)][K/128]; row: [groupsB][K/128][ld(N)]
   int b_row;             // 1: per-row (128x1) B scales
+  int b_mn_major;        // 1: B given as [K][N] (N contiguous), block scales [K/128][ceil(N/128)]
   void* C;               // [groupsC][rows][N]
   int out_f32;
   int accumulate;

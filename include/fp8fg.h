@@ -188,6 +188,27 @@ FP8FG_API int fp8_gemm_dense_quant(const uint8_t* A, const float* sA, const uint
                                    void* workspace, size_t workspace_bytes, fp8fg_stream_t stream);
 
 /*
+ * fp8_gemm_dgrad -- data gradient of a Linear layer whose forward pass is
+ * Y[M][N] = X[M][K] W[N][K]^T:  dX[M][K] = dY[M][N] W[N][K], all in FP8
+ * (DeepSeek-V3 report excerpt, page 1, paragraph 3: Fprop, Dgrad and Wgrad
+ * run as FP8 GEMMs; page 2, paragraph 3: the request for transposed-GEMM
+ * support). W is read as its own transpose straight from the forward
+ * pass's E4M3 bytes and 128x128 block scales (a block's scale does not
+ * change under transposition); no transposed copy is made.
+ *
+ *   dY    [M][N] E4M3, s_dY [N/128][ld(M)]: dY quantized per 1x128 tile
+ *         along N (fp8_quant_1x128)
+ *   W     [N][K] E4M3, sW [N/128][K/128]: as fp8_quant_128x128 wrote them
+ *   dX    [M][K] of out_dtype (BF16 or FP32), written (accumulate = 1:
+ *         dX += result, FP32 only)
+ *   workspace  as fp8_gemm_dense with (M, K, N): fp8fg_gemm_workspace_size(M, K, N)
+ * Requires N % 128 == 0, K % 16 == 0, 16-byte aligned dY, W, dX, s_dY.
+ */
+FP8FG_API int fp8_gemm_dgrad(const uint8_t* dY, const float* s_dY, const uint8_t* W, const float* sW, void* dX,
+                             int out_dtype, int accumulate, int64_t M, int64_t N, int64_t K,
+                             void* workspace, size_t workspace_bytes, fp8fg_stream_t stream);
+
+/*
  * fp8_gemm_dense_noalloc -- fp8_gemm_dense for callers that cannot allocate
  * device memory. (No counterpart in the paper: a deployment convenience of
  * this library.) Some callers only receive device pointers from a host

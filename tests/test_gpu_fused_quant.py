@@ -35,7 +35,7 @@ def _operands(M, N, K, seed):
 
 @pytest.mark.parametrize("M,N,K,pow2", [
     (256, 512, 512, False),
-    (200, 384, 1024, True),     # ragged rows, power-of-2 scales
+    (200, 384, 1024, True),     # ragged rows, power-of-2 scales; N ends halfway through a 256-column tile
     (64, 1024, 2048, False),    # decode-sized: K split over the SMs (Stream-K)
     (1024, 2048, 1024, False),  # several tiles per CTA
 ])
@@ -70,6 +70,21 @@ def test_fused_quant(lib, M, N, K, pow2):
     bound = (2.0 ** -4 + 1e-2) * np.abs(cref) + np.repeat(sn.T, 128, axis=1) * 2.0 ** -9 + \
         1e-2 * np.sqrt(np.mean(cref ** 2))
     assert np.all(err <= bound), f"{int((err > bound).sum())} dequantized values outside E4M3 rounding of Cref"
+
+
+def test_fused_quant_writes_nothing_past_its_outputs(lib):
+    # N = 384 leaves the last 256-column tile half empty: its second half has
+    # no codes or scales to write. Canaries after q and s must survive.
+    M, N, K = 256, 384, 1024
+    qa, sa, qb, sb, qa_d, sa_d, qb_d, sb_d = _operands(M, N, K, 5201)
+    qbuf = torch.full((M * N + 4096,), 0x5A, dtype=torch.uint8, device="cuda")
+    sbuf = torch.full(((N // 128) * M + 4096,), -7.0, dtype=torch.float32, device="cuda")
+    q = qbuf[:M * N].view(M, N)
+    s = sbuf[:(N // 128) * M].view(N // 128, M)
+    lib.fp8_gemm_dense_quant_out(qa_d, sa_d, qb_d, sb_d, q, s, workspace=lib.gemm_workspace(M, N, K))
+    lib.check()
+    assert torch.all(qbuf[M * N:] == 0x5A), "codes written past q"
+    assert torch.all(sbuf[(N // 128) * M:] == -7.0), "scales written past s"
 
 
 def test_fused_quant_without_bf16_output(lib):
