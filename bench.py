@@ -55,9 +55,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # reported traffic is null. Writes sit below M*N*2 because output lines still
 # in L2 when the kernel ends are written back after it.
 NCU_TRAFFIC = {
-    "kernel_sha": "cb0c247e1a6de545",
-    "per_launch": {2112: 45523200 + 1278208, 24576: 210401280 + 180621568,
-                   7168: 83070464 + 37059072, 4096: 60042752 + 11343872},
+    "kernel_sha": "db9b6da0994af8b8",
+    "per_launch": {2112: 45538048 + 708096, 24576: 213254144 + 180313344,
+                   7168: 83710208 + 37388544, 4096: 60657152 + 11906560},
 }
 
 
@@ -87,7 +87,7 @@ def table1_gbs(M, N, K, tflops):
 
 def kernel_sha():
     h = hashlib.sha256()
-    for f in ("gemm.cu", "common.cuh"):
+    for f in ("gemm.cu", "gemm_common.cuh", "common.cuh", "quant_math.cuh"):
         h.update(open(os.path.join(ROOT, "fp8_fine_grained_24_b300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
