@@ -512,6 +512,7 @@ CONFIG_CASES = (
     ("gemm_then_quant", (4096, 7168, 7168), None),
     ("dgrad", (4096, 7168, 7168), None),
     ("wgrad_dense", (4096, 4096, 7168), None),
+    ("wgrad_dense_bs", (4096, 4096, 7168), None),
 )
 
 
@@ -631,6 +632,7 @@ def time_case(case, dims, src="e4m3", steps=20, warmup=5, graph_reps=10, rotate=
     gemm_then_quant M,N,K  the unfused pair: dense GEMM (bf16 out), then fp8_quant_1x128
     dgrad M,N,K       data gradient dX[M,K] = dY[M,N] W[N,K] (W read MN-major), bf16 out
     wgrad_dense T,N,C dense weight gradient dW[N,C] += G^T X over T tokens (128x1 pow2, FP32 accumulate)
+    wgrad_dense_bs T,N,C  the same with the power-of-two scales applied in the tensor core (block-scaled MMA)
     contig E,T,N,K    grouped-contiguous MoE GEMM: T tokens routed by Zipf(1.1) counts
     masked E,M,N,K    grouped-masked MoE GEMM: uniform counts up to M tokens per expert
     wgrad E,T,N,C     masked-K weight gradient dW_e = G_e^T X_e (128x1 pow2 operands, FP32 out)
@@ -689,16 +691,18 @@ def time_case(case, dims, src="e4m3", steps=20, warmup=5, graph_reps=10, rotate=
             ws = None if (not workspace) else fg.gemm_workspace(M, K, N, device=dev)
             return (lambda: fg.fp8_gemm_dgrad_out(qdy, sdy, qw, sw, dx, workspace=ws), gemm_bytes(M, K, N),
                     gemm_flops(M, K, N))
-        if case == "wgrad_dense":
-            # dW[N, C] += G^T X over T tokens: both operands 128x1 (pow2), FP32 accumulate
+        if case in ("wgrad_dense", "wgrad_dense_bs"):
+            # dW[N, C] += G^T X over T tokens: both operands 128x1 (pow2), FP32
+            # accumulate; _bs applies the power-of-two scales in the tensor core
             T, N, C = dims
+            kind = fg.SCALE_ROW_POW2 if case == "wgrad_dense_bs" else fg.SCALE_ROW
             qgT, sgT = fg.fp8_requant_128x1(wl.normal((T, N), seed, device=dev, dtype=torch.bfloat16), pow2=True)
             qx, sx = fg.fp8_quant_1x128(wl.activations(T, C, seed + 1, device=dev))
             qxT, sxT = fg.fp8_requant_128x1(qx.view(torch.float8_e4m3fn), sx, pow2=True)
             dw = torch.zeros((N, C), dtype=torch.float32, device=dev)
             ws = None if (not workspace) else fg.gemm_workspace(N, C, T, device=dev)
             nb = T * (N + C) + 2 * (T // 128) * (N + C) * 4 + 2 * N * C * 4   # dW read and written
-            return (lambda: fg.fp8_gemm_dense_out(qgT, sgT, qxT, sxT, dw, b_scale_kind=fg.SCALE_ROW, accumulate=True,
+            return (lambda: fg.fp8_gemm_dense_out(qgT, sgT, qxT, sxT, dw, b_scale_kind=kind, accumulate=True,
                                                   workspace=ws), nb, 2.0 * T * N * C)
         if case == "contig":
             E, T, N, K = dims
@@ -837,7 +841,8 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--src", choices=["e4m3", "bf16", "fp32"], default="e4m3",
                     help="requant case: source type (E4M3 with 1x128 scales, BF16 or FP32)")
-    ap.add_argument("--case", choices=["gemm", "gemm_quant", "gemm_then_quant", "dgrad", "wgrad_dense", "contig",
+    ap.add_argument("--case", choices=["gemm", "gemm_quant", "gemm_then_quant", "dgrad", "wgrad_dense",
+                                       "wgrad_dense_bs", "contig",
                                        "masked", "wgrad", "quant1x128", "quant128x128", "requant"],
                     default=None,
                     help="time a single kernel on --shape instead of the full step")

@@ -62,7 +62,7 @@ ERR_CUDA = -4
 ERR_TIMEOUT = -5
 
 BF16, FP32, E4M3 = 0, 1, 2
-SCALE_BLOCK128, SCALE_ROW = 0, 1
+SCALE_BLOCK128, SCALE_ROW, SCALE_ROW_POW2 = 0, 1, 2
 MASK_ROWS, MASK_K = 0, 1
 
 _c_i64 = ctypes.c_int64

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libfp8fg.so")
 OBJDIR = os.path.join(ROOT, "_build")
-SOURCES = ("api.cu", "quant.cu", "gemm.cu", "gemm_pair.cu", "noalloc.cu", "study.cu", "tmap.cu")
+SOURCES = ("api.cu", "quant.cu", "gemm.cu", "gemm_pair.cu", "gemm_bs.cu", "noalloc.cu", "study.cu", "tmap.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", INCLUDE]

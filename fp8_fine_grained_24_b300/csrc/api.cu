@@ -101,8 +101,9 @@ int check_gemm_common(const void* A, const void* sA, const void* B, const void* 
   if (rows < 0 || N < 0 || K < 0) return fail(FP8FG_ERR_INVALID_ARG, "negative size");
   if (out_dtype != FP8FG_BF16 && out_dtype != FP8FG_FP32)
     return fail(FP8FG_ERR_INVALID_ARG, "out_dtype must be FP8FG_BF16 or FP8FG_FP32");
-  if (b_scale_kind != FP8FG_SCALE_BLOCK128 && b_scale_kind != FP8FG_SCALE_ROW)
-    return fail(FP8FG_ERR_INVALID_ARG, "b_scale_kind must be FP8FG_SCALE_BLOCK128 or FP8FG_SCALE_ROW");
+  if (b_scale_kind != FP8FG_SCALE_BLOCK128 && b_scale_kind != FP8FG_SCALE_ROW && b_scale_kind != FP8FG_SCALE_ROW_POW2)
+    return fail(FP8FG_ERR_INVALID_ARG,
+                "b_scale_kind must be FP8FG_SCALE_BLOCK128, FP8FG_SCALE_ROW or FP8FG_SCALE_ROW_POW2");
   if (accumulate != 0 && accumulate != 1) return fail(FP8FG_ERR_INVALID_ARG, "accumulate must be 0 or 1");
   if (accumulate && out_dtype != FP8FG_FP32)
     return fail(FP8FG_ERR_INVALID_ARG, "accumulate=1 needs FP32 output");
@@ -112,7 +113,7 @@ int check_gemm_common(const void* A, const void* sA, const void* B, const void* 
   if (!A || !sA || !B || !sB || !C) return fail(FP8FG_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(A) || !aligned16(B) || !aligned16(C) || !aligned16(sA))
     return fail(FP8FG_ERR_MISALIGNED, "A, B, C and sA must be 16-byte aligned");
-  if (b_scale_kind == FP8FG_SCALE_ROW ? !aligned16(sB) : !aligned4(sB))
+  if (b_scale_kind != FP8FG_SCALE_BLOCK128 ? !aligned16(sB) : !aligned4(sB))
     return fail(FP8FG_ERR_MISALIGNED, "sB must be 16-byte aligned (per-row scales) or 4-byte aligned");
   return FP8FG_OK;
 }
@@ -229,7 +230,8 @@ int fp8_gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const fl
   fp8fg::GemmProblem p{};
   p.mode = fp8fg::kModeDense;
   p.A = A; p.sA = sA; p.B = B; p.sB = sB;
-  p.b_row = b_scale_kind == FP8FG_SCALE_ROW;
+  p.b_row = b_scale_kind != FP8FG_SCALE_BLOCK128;
+  p.b_scale_pow2 = b_scale_kind == FP8FG_SCALE_ROW_POW2;
   p.C = C; p.out_f32 = out_dtype == FP8FG_FP32; p.accumulate = accumulate;
   p.rows = M; p.N = N; p.K = K; p.groups = 1; p.groupsB = 1;
   if (workspace != nullptr && !aligned16(workspace))
@@ -331,7 +333,7 @@ int fp8_gemm_grouped_masked(const uint8_t* A, const float* sA, const uint8_t* B,
   if (E > kMaxDim) return fail(FP8FG_ERR_UNSUPPORTED_SHAPE, "too many experts");
   fp8fg::GemmProblem p{};
   p.mode = mask_dim == FP8FG_MASK_ROWS ? fp8fg::kModeMaskedRows : fp8fg::kModeMaskedK;
-  p.A = A; p.sA = sA; p.B = B; p.sB = sB; p.b_row = b_scale_kind == FP8FG_SCALE_ROW;
+  p.A = A; p.sA = sA; p.B = B; p.sB = sB; p.b_row = b_scale_kind != FP8FG_SCALE_BLOCK128;
   p.C = C; p.out_f32 = out_dtype == FP8FG_FP32; p.accumulate = accumulate;
   p.rows = M_max; p.N = N; p.K = K; p.groups = E; p.groupsB = E;
   p.masked = masked_m;
@@ -351,6 +353,9 @@ int fp8fg_check(fp8fg_stream_t stream) {
     const uint32_t zero = 0;
     e = cudaMemcpy(st->status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+    if (word == fp8fg::kStatusScaleNotPow2)
+      return fail(FP8FG_ERR_INVALID_ARG,
+                  "a GEMM with FP8FG_SCALE_ROW_POW2 was given a scale that is not a power of two (its result is wrong)");
     return fail(FP8FG_ERR_TIMEOUT, "a bounded device wait expired (code %u)", word);
   }
   return FP8FG_OK;

@@ -22,6 +22,8 @@ enum : uint32_t {
   kStatusTimeoutMma = 2,
   kStatusTimeoutEpilogue = 3,
   kStatusTimeoutDrain = 4,
+  // (5-7: the quantizers' timeouts)
+  kStatusScaleNotPow2 = 8,  // a block-scaled GEMM was given a scale that is not a power of two
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -280,6 +282,46 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
+}
+
+// Store 32 lanes x N consecutive 32-bit columns from registers (thread i of
+// the warp writes lane taddr.lane + i); the column address is a multiple of
+// N. tmem_wait_st waits until this thread's stores have completed.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&v)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D[tmem] (+)= (A * 2^sfa) * (B * 2^sfb)^T: E4M3 x E4M3 -> FP32 with UE8M0
+// scale factors from TMEM, one per row of A and per row of B for the
+// instruction's K of 32 (block_scale, scale_vec::1X). Measured layout on
+// sm_103a (M = 128): row m of A takes lane m, column sfa + m/32; row n of
+// B, for the output rows of lane quadrant q, lane 32q + n%32, column
+// sfb + n/32; the byte within the 32-bit cell is the scale-factor ID of the
+// instruction descriptor (0 here).
+__device__ __forceinline__ void mma_mxf8_bs(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor for kind::mxf8f6f4 with block scaling: A and B
+// E4M3, K-major, N >> 3 in bits 17-22, UE8M0 scale type (bit 23), M >> 4 in
+// bits 24-28, scale-factor IDs 0 (bits 4-5 for B, 29-30 for A).
+__host__ __device__ constexpr uint32_t mxf8_idesc(int m, int n) {
+  return (1u << 23) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor for a K-major operand tile whose rows are

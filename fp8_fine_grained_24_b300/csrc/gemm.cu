@@ -986,6 +986,7 @@ void gemm_workspace_zero_range(int mode, int64_t rows, int64_t N, int64_t K, int
 
 cudaError_t launch_gemm(const GemmProblem& p, uint32_t* status, uint64_t wait_limit_ns, int debug_skip_fill,
                         int num_sms, cudaStream_t stream, const char** detail) {
+  if (bs_gemm_eligible(p)) return launch_gemm_bs(p, status, wait_limit_ns, debug_skip_fill, num_sms, stream, detail);
   if (p.q_out == nullptr && !p.b_mn_major && pair_gemm_eligible(p, num_sms))
     return launch_gemm_pair(p, status, wait_limit_ns, debug_skip_fill, stream, detail);
   int bn = pick_bn(p.mode, p.rows, p.q_out != nullptr);

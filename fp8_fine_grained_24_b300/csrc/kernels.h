@@ -39,6 +39,7 @@ struct GemmProblem {
   const float* sB;       // block: [groupsB][ceil(N/128)][K/128]; row: [groupsB][K/128][ld(N)]
   int b_row;             // 1: per-row (128x1) B scales
   int b_mn_major;        // 1: B given as [K][N] (N contiguous), block scales [K/128][ceil(N/128)]
+  int b_scale_pow2;      // 1 (with b_row): both operands' row scales are powers of two
   void* C;               // [groupsC][rows][N]
   int out_f32;
   int accumulate;
@@ -89,6 +90,12 @@ bool pair_gemm_eligible(const GemmProblem& p, int num_sms);
 void set_pair_gemm_enabled(bool on);
 cudaError_t launch_gemm_pair(const GemmProblem& p, uint32_t* status, uint64_t wait_limit_ns, int debug_skip_fill,
                              cudaStream_t stream, const char** detail);
+
+// The block-scaled GEMM (gemm_bs.cu): power-of-two row scales on both
+// operands applied inside the tensor core, dense layout, FP32 output.
+bool bs_gemm_eligible(const GemmProblem& p);
+cudaError_t launch_gemm_bs(const GemmProblem& p, uint32_t* status, uint64_t wait_limit_ns, int debug_skip_fill,
+                           int num_sms, cudaStream_t stream, const char** detail);
 
 // Tensor-core accumulation study (see study.cu): D[128][N] = A[128][K] B[N][K]^T
 // on unscaled E4M3 codes, the MMA accumulator restarted every `interval` K.

@@ -72,6 +72,12 @@ typedef struct CUstream_st* fp8fg_stream_t; /* identical to cudaStream_t */
 /* how the B operand of a GEMM is scaled */
 #define FP8FG_SCALE_BLOCK128 0 /* sB[ceil(N/128)][K/128]: one scale per 128x128 block   */
 #define FP8FG_SCALE_ROW      1 /* sB[K/128][ld(N)]: one scale per row per 128 K (128x1) */
+#define FP8FG_SCALE_ROW_POW2 2 /* as FP8FG_SCALE_ROW, and every scale of A and of B is a power of
+                                * two (fp8_requant_128x1 with pow2 = 1): dense FP32-output GEMMs
+                                * then apply the scales inside the tensor core (block-scaled MMA,
+                                * UE8M0) instead of promoting partial sums; other forms use the
+                                * FP8FG_SCALE_ROW path. A scale that is not a power of two makes
+                                * fp8fg_check report FP8FG_ERR_INVALID_ARG. */
 
 /* what masked_m limits in fp8_gemm_grouped_masked */
 #define FP8FG_MASK_ROWS 0 /* rows of A (forward / decode MoE)            */
