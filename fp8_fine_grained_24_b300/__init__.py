@@ -150,6 +150,15 @@ def debug_set(key: int, value: int):
     _check(lib.fp8fg_debug_set(int(key), int(value)))
 
 
+# K split of decode-sized dense GEMMs (fp8fg_debug_set key 4)
+SPLIT_AUTO, SPLIT_STREAM, SPLIT_CLUSTER = 0, 1, 2
+
+
+def set_split_policy(policy: int):
+    """Automatic, Stream-K over the workspace only, or the cluster split wherever it applies."""
+    debug_set(4, policy)
+
+
 # ---------------------------------------------------------------- quantizers
 def fp8_quant_1x128_out(x, q, s, pow2=False, stream=None):
     M, K = x.shape
@@ -206,7 +215,11 @@ def fp8_requant_128x1(src, s_src=None, valid_rows=None, pow2=False, stream=None)
 
 # ---------------------------------------------------------------- GEMMs
 def gemm_workspace_size(M: int, N: int, K: int) -> int:
-    """Stream-K workspace bytes for a dense GEMM on the current device (0: none)."""
+    """Stream-K workspace bytes for a dense GEMM on the current device (0: none).
+
+    The cluster split, which the automatic policy prefers for decode-sized
+    problems, uses no workspace; the size covers the Stream-K plan that the
+    policy may choose instead."""
     return int(lib.fp8fg_gemm_workspace_size(M, N, K))
 
 
@@ -327,7 +340,8 @@ def study_mma_accumulation(a, b, interval, stream=None):
 
 
 __all__ = [
-    "lib", "LIB_PATH", "Fp8fgError", "scale_ld", "version", "check", "debug_set",
+    "lib", "LIB_PATH", "Fp8fgError", "scale_ld", "version", "check", "debug_set", "set_split_policy",
+    "SPLIT_AUTO", "SPLIT_STREAM", "SPLIT_CLUSTER",
     "fp8_quant_1x128", "fp8_quant_1x128_out", "fp8_quant_128x128", "fp8_quant_128x128_out",
     "fp8_requant_128x1", "fp8_requant_128x1_out", "gemm_workspace_size", "gemm_workspace",
     "fp8_gemm_dense", "fp8_gemm_dense_out", "fp8_gemm_dense_quant", "fp8_gemm_dense_quant_out",

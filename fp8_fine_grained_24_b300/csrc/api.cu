@@ -393,6 +393,10 @@ int fp8fg_debug_set(int key, int64_t value) {
       if (value != 0 && value != 1) return fail(FP8FG_ERR_INVALID_ARG, "value must be 0 or 1");
       fp8fg::set_pair_gemm_enabled(value == 1);
       return FP8FG_OK;
+    case 4:
+      if (value < 0 || value > 2) return fail(FP8FG_ERR_INVALID_ARG, "value must be 0, 1 or 2");
+      fp8fg::set_split_policy(static_cast<int>(value));
+      return FP8FG_OK;
     default:
       return fail(FP8FG_ERR_INVALID_ARG, "unknown debug key %d", key);
   }

@@ -187,25 +187,46 @@ struct Work {
   int t, u, end;
 };
 
-template <bool kSK>
+// How a launch splits K: not at all (whole tiles), Stream-K (unit ranges
+// cut at tile boundaries, partials summed through the workspace), or over
+// the CTAs of a cluster (one tile per cluster, partials summed through
+// distributed shared memory).
+enum : int { kSplitNone = 0, kSplitStream = 1, kSplitCluster = 2 };
+
+template <int kSK>
 __device__ __forceinline__ Work work_begin(const KArgs& a) {
   Work w;
   w.t = blockIdx.x;
   w.u = w.end = 0;
 
-  if constexpr (kSK) {
+  if constexpr (kSK == kSplitStream) {
     const int64_t u = static_cast<int64_t>(blockIdx.x) * a.sk_per_cta;
     const int64_t e = u + a.sk_per_cta;
     w.u = static_cast<int>(u < a.sk_units ? u : a.sk_units);
     w.end = static_cast<int>(e < a.sk_units ? e : a.sk_units);
+  } else if constexpr (kSK == kSplitCluster) {
+    // cluster t computes tile t; its CTA r (blockIdx.x % cl_split, the
+    // rank: the clusters tile the grid along x) takes the r-th K range
+    const int r = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.cl_split));
+    w.t = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.cl_split));
+    w.u = static_cast<int>(static_cast<int64_t>(r) * a.KB / a.cl_split);
+    w.end = static_cast<int>(static_cast<int64_t>(r + 1) * a.KB / a.cl_split);
   }
   return w;
 }
 
 // kCompact (masked rows only): the tiles are the active ones.
-template <int BN, bool kSK, bool kCompact>
+template <int BN, int kSK, bool kCompact>
 __device__ __forceinline__ bool work_next(const KArgs& a, Work& w, Tile& ti) {
-  const int dp = kSK ? a.dp_tiles : a.num_tiles;
+  if constexpr (kSK == kSplitCluster) {
+    if (w.u >= w.end) return false;
+    ti = decode_tile<BN>(a, w.t);
+    ti.kb0 = w.u;
+    ti.kbc = w.end - w.u;
+    w.u = w.end;
+    return true;
+  }
+  const int dp = kSK == kSplitStream ? a.dp_tiles : a.num_tiles;
   if constexpr (kCompact) {
     if (!decode_masked_tile<BN>(a, w.t, ti)) return false;
     w.t += gridDim.x;
@@ -216,7 +237,7 @@ __device__ __forceinline__ bool work_next(const KArgs& a, Work& w, Tile& ti) {
     w.t += gridDim.x;
     return true;
   }
-  if constexpr (kSK) {
+  if constexpr (kSK == kSplitStream) {
     if (w.u < w.end) {
       const int tt = w.u / a.KB;
       const int kb0 = w.u - tt * a.KB;
@@ -286,6 +307,99 @@ __device__ __forceinline__ bool sk_reduce(const KArgs& a, const Tile& ti, int ro
   return true;
 }
 
+// Cluster split. The tile's 16 column chunks of 8 are divided among the S
+// CTAs of its cluster, CTA r owning chunks [b(r), b(r+1)), b(r) =
+// floor(16 r / S). Once every CTA of the cluster is past its K loop (a
+// cluster barrier: from then on no stage of any of them is in use), each
+// epilogue thread stores its row's FP32 partial sums, chunk by chunk, into
+// the shared memory of the chunk's owner, in the slot of the sending rank:
+// slot q holds BM rows of kPitch(S) floats. After a second barrier (release
+// and acquire: the stores have landed) every CTA sums its own chunks over
+// the S slots in rank order, so the result does not depend on timing, and
+// stores them. Nothing reads another CTA's shared memory after that
+// barrier, so a CTA may then leave.
+// kPitch: the owner's widest share, plus 4 floats that make the row pitch
+// an odd number of 16-byte units, so that a warp's 32 rows land on
+// distinct bank groups.
+template <int BN>
+struct ClusterPart {
+  static constexpr int kChunks = BN / 8;
+  static constexpr int kMaxSplit = 8;  // portable cluster size
+  static __host__ __device__ constexpr int pitch(int S) { return (kChunks + S - 1) / S * 8 + 4; }
+  static __host__ __device__ constexpr int bytes(int S) { return S * BM * pitch(S) * 4; }
+  static constexpr int max_bytes(int S = 2) {
+    return S > kMaxSplit ? 0 : (bytes(S) > max_bytes(S + 1) ? bytes(S) : max_bytes(S + 1));
+  }
+  // the owner of chunk ch: the r with b(r) <= ch < b(r + 1)
+  static __device__ __forceinline__ int owner(int ch, int S) { return (ch * S + S - 1) / kChunks; }
+  static __device__ __forceinline__ int first(int r, int S) { return r * kChunks / S; }
+};
+
+// One epilogue thread's row of partial sums (columns col0 .. col0 + NC of
+// the tile) to the chunks' owners.
+template <int BN, int NC>
+__device__ __forceinline__ void cluster_push(const KArgs& a, const Tile& ti, int row_in_tile, int col0,
+                                             uint32_t sbase, const float (&acc)[NC]) {
+  using P = ClusterPart<BN>;
+  if (ti.m0 + row_in_tile >= a.rows) return;  // rows past the end are never stored
+  const int S = a.cl_split;
+  const int me = static_cast<int>(cluster_ctarank());
+  const int pitch = P::pitch(S);
+#pragma unroll
+  for (int k = 0; k < NC / 8; ++k) {
+    const int ch = col0 / 8 + k;
+    const int r = P::owner(ch, S);
+    const int lc = ch - P::first(r, S);
+    const uint32_t dst = map_to_cta(sbase, static_cast<uint32_t>(r)) +
+                         static_cast<uint32_t>(((me * BM + row_in_tile) * pitch + lc * 8) * 4);
+    st_cluster_f4(dst, acc[8 * k], acc[8 * k + 1], acc[8 * k + 2], acc[8 * k + 3]);
+    st_cluster_f4(dst + 16, acc[8 * k + 4], acc[8 * k + 5], acc[8 * k + 6], acc[8 * k + 7]);
+  }
+}
+
+// This CTA's chunks of the tile: the sum over the S slots, stored to C.
+template <int BN, bool kF32>
+__device__ __forceinline__ void cluster_reduce_store(const KArgs& a, const Tile& ti, const float* part) {
+  using P = ClusterPart<BN>;
+  const int S = a.cl_split;
+  const int r = static_cast<int>(cluster_ctarank());
+  const int c_begin = P::first(r, S), nch = P::first(r + 1, S) - c_begin;
+  const int pitch = P::pitch(S);
+  const int rows = a.rows - ti.m0 < BM ? a.rows - ti.m0 : BM;
+  for (int i = threadIdx.x; i < rows * nch; i += blockDim.x) {
+    const int row = i / nch;
+    const int lc = i - row * nch;
+    const int col = ti.n0 + (c_begin + lc) * 8;
+    if (col >= a.N) continue;  // N % 8 == 0: a chunk is wholly inside or outside
+    const float* src = part + row * pitch + lc * 8;
+    float4 lo = make_float4(0.0f, 0.0f, 0.0f, 0.0f), hi = lo;
+    for (int q = 0; q < S; ++q) {
+      const float4 x = *reinterpret_cast<const float4*>(src + q * BM * pitch);
+      const float4 y = *reinterpret_cast<const float4*>(src + q * BM * pitch + 4);
+      lo.x += x.x; lo.y += x.y; lo.z += x.z; lo.w += x.w;
+      hi.x += y.x; hi.y += y.y; hi.z += y.z; hi.w += y.w;
+    }
+    const int64_t o = static_cast<int64_t>(ti.m0 + row) * a.ldc + col;
+    if constexpr (kF32) {
+      float4* c = reinterpret_cast<float4*>(static_cast<float*>(a.C) + o);
+      if (a.accumulate) {
+        const float4 u = c[0], v = c[1];
+        lo.x += u.x; lo.y += u.y; lo.z += u.z; lo.w += u.w;
+        hi.x += v.x; hi.y += v.y; hi.z += v.z; hi.w += v.w;
+      }
+      c[0] = lo;
+      c[1] = hi;
+    } else {
+      uint4 v;
+      v.x = pack_bf16x2(lo.x, lo.y);
+      v.y = pack_bf16x2(lo.z, lo.w);
+      v.z = pack_bf16x2(hi.x, hi.y);
+      v.w = pack_bf16x2(hi.z, hi.w);
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.C) + o) = v;
+    }
+  }
+}
+
 // Fused 1x128 quantization of one epilogue warp's 32 rows x 128 columns of
 // C (DeepSeek-V3 report excerpt, page 1, paragraph 3: activations are
 // quantized per 1x128 tile; the DeepGEMM article's call to fuse the FP8 cast
@@ -343,7 +457,7 @@ __device__ __forceinline__ void quant_store_tile(const KArgs& a, const Tile& ti,
 // output, or B read MN-major (the weight as its own transpose).
 enum : int { kVarPlain = 0, kVarQuant = 1, kVarBT = 2 };
 
-template <int BN, bool kBRow, bool kF32, bool kSplit, bool kCompact, int kVar>
+template <int BN, bool kBRow, bool kF32, int kSplit, bool kCompact, int kVar>
 __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
@@ -354,7 +468,11 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   static_assert(!kQ || (BN == 256 && !kBRow && !kF32 && !kCompact),
                 "fused quantization: 128-column warps of BF16 output, dense layout");
   static_assert(!kBT || (BN != 192 && !kBRow && !kCompact), "MN-major B: 128-column boxes, block scales");
+  static_assert(kSplit != kSplitCluster || (BN == 128 && !kQ && !kCompact),
+                "cluster split: 128-column tiles, row-by-row stores, dense layout");
   using C = Cfg<BN>;
+  static_assert(kSplit != kSplitCluster || ClusterPart<BN>::max_bytes() <= C::kOffEpi,
+                "the partial tiles fit in the pipeline stages");
   constexpr int S = C::kStages;
   constexpr int NB = C::kAccBufs;
   extern __shared__ uint8_t smem_raw[];
@@ -405,7 +523,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
    if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      constexpr uint32_t tx = C::kABytes + C::kBBytes + C::kSABytes + (kBRow ? C::kSBBytes : 0);
+      const uint32_t tx = static_cast<uint32_t>(a.a_rows_box) * BK + C::kBBytes + C::kSABytes + (kBRow ? C::kSBBytes : 0);
       uint32_t it = 0;
       bool ok = true;
       Work wk = work_begin<kSplit>(a);
@@ -499,6 +617,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     float acc[NC];
     uint32_t it = 0;
     bool ok = true;
+    bool pushed = false;  // cluster split: this warp has passed the first cluster barrier
     // BF16 tiles go out through shared-memory staging and TMA stores
     constexpr bool kStage = C::kTmaStore;
     int held = -1;  // pipeline stage kept for staging (kStage, warps < kBorrowWarps)
@@ -572,9 +691,18 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       }
       if (!ok) break;
       bool store = !(a.accumulate && ti.kbc == 0);
-      if constexpr (kSplit) {
+      if constexpr (kSplit == kSplitStream) {
         // a Stream-K piece of a split tile: only the last to arrive stores
         if (ti.kbc != a.KB) store = sk_reduce<NC, C::kEpiWarps>(a, ti, row_in_tile, ew, lane, acc);
+      } else if constexpr (kSplit == kSplitCluster) {
+        // first cluster barrier: every CTA of the cluster is past its K
+        // loop (its MMAs complete, its fills landed), so the partials may
+        // go into the owners' stages
+        fence_async_shared();
+        cluster_sync();
+        pushed = true;
+        cluster_push<BN, NC>(a, ti, row_in_tile, col0, sbase, acc);
+        store = false;
       }
       bool staged = false;
       if (store) {
@@ -615,8 +743,30 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     if constexpr (kStage) {
       if (lane == 0) bulk_wait_all();
     }
+    if constexpr (kSplit == kSplitCluster) {
+      // a warp that left its loop early (a timed-out wait) still takes part
+      // in the first barrier, so that no CTA of the cluster waits forever
+      if (!pushed) {
+        __syncwarp();
+        fence_async_shared();
+        cluster_sync();
+      }
+    }
   }
 
+  if constexpr (kSplit == kSplitCluster) {
+    // the producer and MMA warps take part in the first barrier here; then
+    // every thread: the second barrier (all partials have landed), and this
+    // CTA's share of the tile
+    __syncwarp();
+    if (warp < C::kEpiWarp0) {
+      fence_async_shared();
+      cluster_sync();
+    }
+    cluster_sync();
+    cluster_reduce_store<BN, kF32>(a, decode_tile<BN>(a, static_cast<int>(blockIdx.x / a.cl_split)),
+                                   reinterpret_cast<const float*>(smem));
+  }
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -628,7 +778,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
 
 // Raise the kernel's dynamic shared-memory limit once per device (the call
 // costs tens of microseconds of host time, so it is not repeated per launch).
-template <int BN, bool kBRow, bool kF32, bool kSplit, bool kCompact, int kVar = kVarPlain>
+template <int BN, bool kBRow, bool kF32, int kSplit, bool kCompact, int kVar = kVarPlain>
 cudaError_t ensure_smem_attr() {
   static std::atomic<uint64_t> done{0};
   int dev = 0;
@@ -720,13 +870,86 @@ Plan plan_gemm(int mode, int64_t rows, int64_t N, int64_t K, int64_t groups, int
   return p;
 }
 
+// Split policy for decode-sized dense problems: automatic (the cluster
+// split wherever it applies, else Stream-K when a workspace is given),
+// Stream-K only, or the cluster split whenever it applies. FP8FG_SPLIT=
+// stream|cluster sets it at load; fp8fg_debug_set(4, ...) at run time.
+enum : int { kPolicyAuto = 0, kPolicyStream = 1, kPolicyCluster = 2 };
+std::atomic<int> g_split_policy{[] {
+  const char* v = std::getenv("FP8FG_SPLIT");
+  if (v && std::strcmp(v, "stream") == 0) return static_cast<int>(kPolicyStream);
+  if (v && std::strcmp(v, "cluster") == 0) return static_cast<int>(kPolicyCluster);
+  return static_cast<int>(kPolicyAuto);
+}()};
+
+int split_policy() { return g_split_policy.load(std::memory_order_relaxed); }
+
+// Clusters of `size` CTAs of `fn` that fit on the device at once (cached per
+// device and size; the kernels that share a tile configuration have the same
+// threads and shared memory, so one query serves them all).
+template <class Fn>
+cudaError_t cluster_capacity(Fn fn, int size, int* fit) {
+  static std::atomic<int> cache[64][ClusterPart<128>::kMaxSplit + 1];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::atomic<int>& slot = cache[dev & 63][size];
+  const int v = slot.load(std::memory_order_acquire);
+  if (v > 0) {
+    *fit = v - 1;
+    return cudaSuccess;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(size));
+  cfg.blockDim = dim3(Cfg<128>::kThreads);
+  cfg.dynamicSmemBytes = Cfg<128>::kSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(size);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+  if (e != cudaSuccess) return e;
+  slot.store(n + 1, std::memory_order_release);
+  *fit = n;
+  return cudaSuccess;
+}
+
+// Cluster split of a decode-sized dense problem (its 128 x 128 tiles at most
+// half the SMs): the largest S <= 8 with S CTAs per tile on the SMs, at
+// least kMinUnits K blocks per CTA, and all tiles' clusters resident at
+// once. *cl = 0 where none applies.
+template <class Fn>
+cudaError_t pick_cluster_split(int mode, int64_t rows, int64_t N, int64_t K, int64_t groups, int num_sms, Fn fn,
+                               int* cl) {
+  *cl = 0;
+  if (mode != kModeDense || groups != 1) return cudaSuccess;
+  const int64_t KB = K / BK;
+  const int64_t tiles = ((rows + BM - 1) / BM) * ((N + 127) / 128);
+  if (tiles <= 0 || tiles * 2 > num_sms) return cudaSuccess;
+  int64_t S = num_sms / tiles;
+  if (S > ClusterPart<128>::kMaxSplit) S = ClusterPart<128>::kMaxSplit;
+  if (S > KB / kMinUnits) S = KB / kMinUnits;
+  for (; S >= 2; --S) {
+    int fit = 0;
+    const cudaError_t e = cluster_capacity(fn, static_cast<int>(S), &fit);
+    if (e != cudaSuccess) return e;
+    if (fit >= tiles) break;
+  }
+  *cl = S >= 2 ? static_cast<int>(S) : 0;
+  return cudaSuccess;
+}
+
 template <int BN>
 bool encode_maps(const GemmProblem& p, MapSet* m) {
   using C = Cfg<BN>;
   const int64_t KB = p.K / BK;
   const int64_t groupsA = (p.mode == kModeMaskedRows || p.mode == kModeMaskedK) ? p.groups : 1;
-  bool ok = make_map(&m->a, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.A, p.K, p.rows, groupsA, p.K, p.rows * p.K, BK, BM,
-                     CU_TENSOR_MAP_SWIZZLE_128B);
+  bool ok = make_map(&m->a, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.A, p.K, p.rows, groupsA, p.K, p.rows * p.K, BK,
+                     a_box_rows(p.rows), CU_TENSOR_MAP_SWIZZLE_128B);
   if (p.b_mn_major)  // B stored [K][N]: boxes of 128 columns x 128 K rows
     ok = ok && make_map(&m->b, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.B, p.N, p.K, p.groupsB, p.N, p.N * p.K, 128, BK,
                         CU_TENSOR_MAP_SWIZZLE_128B);
@@ -823,6 +1046,8 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
   a.sk_units = a.sk_per_cta = a.sk_lcm = 0;
   a.ws_partial = nullptr;
   a.ws_count = nullptr;
+  a.cl_split = 0;
+  a.a_rows_box = a_box_rows(p.rows);
   a.s_out = p.s_out;
   a.ld_s = ld4(p.rows);
   a.pow2_out = p.pow2_out;
@@ -832,8 +1057,9 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
                               p.workspace != nullptr ? p.workspace_bytes : 0);
 
   using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, KArgs);
-  // whole tiles / Stream-K / active tiles of the masked-rows layout
-  KernelFn kernels[3] = {nullptr, nullptr, nullptr};
+  // whole tiles / Stream-K / active tiles of the masked-rows layout / cluster split
+  KernelFn kernels[4] = {nullptr, nullptr, nullptr, nullptr};
+  cudaError_t (*cluster_attr)() = nullptr;
   const bool masked = p.mode == kModeMaskedRows;
   cudaError_t e = cudaSuccess;
   const int variant = p.q_out != nullptr ? 8 : p.b_mn_major ? 10 + (p.out_f32 ? 1 : 0)
@@ -841,12 +1067,16 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
   switch (variant) {
 #define FP8FG_VARIANT(V, R, F)                                                   \
   case V:                                                                        \
-    kernels[0] = fp8_gemm_kernel<BN, R, F, false, false, kVarPlain>;             \
-    kernels[1] = fp8_gemm_kernel<BN, R, F, true, false, kVarPlain>;              \
-    kernels[2] = fp8_gemm_kernel<BN, R, F, false, true, kVarPlain>;              \
-    e = masked ? ensure_smem_attr<BN, R, F, false, true>()                       \
-               : ensure_smem_attr<BN, R, F, false, false>();                     \
-    if (e == cudaSuccess && plan.sk) e = ensure_smem_attr<BN, R, F, true, false>(); \
+    kernels[0] = fp8_gemm_kernel<BN, R, F, kSplitNone, false, kVarPlain>;        \
+    kernels[1] = fp8_gemm_kernel<BN, R, F, kSplitStream, false, kVarPlain>;      \
+    kernels[2] = fp8_gemm_kernel<BN, R, F, kSplitNone, true, kVarPlain>;         \
+    if constexpr (BN == 128) {                                                   \
+      kernels[3] = fp8_gemm_kernel<BN, R, F, kSplitCluster, false, kVarPlain>;   \
+      cluster_attr = ensure_smem_attr<BN, R, F, kSplitCluster, false>;           \
+    }                                                                            \
+    e = masked ? ensure_smem_attr<BN, R, F, kSplitNone, true>()                  \
+               : ensure_smem_attr<BN, R, F, kSplitNone, false>();                \
+    if (e == cudaSuccess && plan.sk) e = ensure_smem_attr<BN, R, F, kSplitStream, false>(); \
     break;
     FP8FG_VARIANT(0, false, false)
     FP8FG_VARIANT(2, false, true)
@@ -856,10 +1086,10 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
     case 8:
       // fused 1x128 quantization of the BF16 output (dense, 128x256 tiles)
       if constexpr (BN == 256) {
-        kernels[0] = fp8_gemm_kernel<BN, false, false, false, false, kVarQuant>;
-        kernels[1] = fp8_gemm_kernel<BN, false, false, true, false, kVarQuant>;
-        e = ensure_smem_attr<BN, false, false, false, false, kVarQuant>();
-        if (e == cudaSuccess && plan.sk) e = ensure_smem_attr<BN, false, false, true, false, kVarQuant>();
+        kernels[0] = fp8_gemm_kernel<BN, false, false, kSplitNone, false, kVarQuant>;
+        kernels[1] = fp8_gemm_kernel<BN, false, false, kSplitStream, false, kVarQuant>;
+        e = ensure_smem_attr<BN, false, false, kSplitNone, false, kVarQuant>();
+        if (e == cudaSuccess && plan.sk) e = ensure_smem_attr<BN, false, false, kSplitStream, false, kVarQuant>();
       } else {
         e = cudaErrorInvalidValue;
       }
@@ -867,10 +1097,14 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
 #define FP8FG_VARIANT_BT(V, F)                                                          \
   case V:                                                                               \
     if constexpr (BN != 192) {                                                          \
-      kernels[0] = fp8_gemm_kernel<BN, false, F, false, false, kVarBT>;                 \
-      kernels[1] = fp8_gemm_kernel<BN, false, F, true, false, kVarBT>;                  \
-      e = ensure_smem_attr<BN, false, F, false, false, kVarBT>();                       \
-      if (e == cudaSuccess && plan.sk) e = ensure_smem_attr<BN, false, F, true, false, kVarBT>(); \
+      kernels[0] = fp8_gemm_kernel<BN, false, F, kSplitNone, false, kVarBT>;            \
+      kernels[1] = fp8_gemm_kernel<BN, false, F, kSplitStream, false, kVarBT>;          \
+      if constexpr (BN == 128) {                                                        \
+        kernels[3] = fp8_gemm_kernel<BN, false, F, kSplitCluster, false, kVarBT>;       \
+        cluster_attr = ensure_smem_attr<BN, false, F, kSplitCluster, false, kVarBT>;    \
+      }                                                                                 \
+      e = ensure_smem_attr<BN, false, F, kSplitNone, false, kVarBT>();                  \
+      if (e == cudaSuccess && plan.sk) e = ensure_smem_attr<BN, false, F, kSplitStream, false, kVarBT>(); \
     } else {                                                                            \
       e = cudaErrorInvalidValue;                                                        \
     }                                                                                   \
@@ -887,7 +1121,22 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
     *detail = "cudaFuncSetAttribute(max dynamic shared memory) failed";
     return e;
   }
-  if (!plan.sk) {
+  // the cluster split where it applies and the policy allows it
+  int cl = 0;
+  const int policy = split_policy();
+  if (kernels[3] != nullptr && policy != kPolicyStream) {
+    e = cluster_attr();
+    if (e == cudaSuccess) e = pick_cluster_split(p.mode, p.rows, p.N, p.K, p.groups, num_sms, kernels[3], &cl);
+    if (e != cudaSuccess) {
+      *detail = "cluster split set-up (shared-memory attribute or cluster occupancy) failed";
+      return e;
+    }
+  }
+  if (cl >= 2 && (policy == kPolicyCluster || policy == kPolicyAuto)) {
+    a.cl_split = cl;
+    e = launch_kernel_cluster(kernels[3], dim3(static_cast<unsigned>(a.num_tiles * cl)), dim3(C::kThreads), C::kSmem,
+                              stream, static_cast<unsigned>(cl), tmA, tmB, tmSA, tmSB, tmC, tmQ, a);
+  } else if (!plan.sk) {
     e = launch_kernel(kernels[masked ? 2 : 0], dim3(plan.grid), dim3(C::kThreads), C::kSmem, stream, tmA, tmB, tmSA,
                       tmSB, tmC, tmQ, a);
   } else {
@@ -925,6 +1174,8 @@ int pick_bn(int mode, int64_t rows, bool quant_out = false) {
 }
 
 }  // namespace
+
+void set_split_policy(int policy) { g_split_policy.store(policy); }
 
 namespace gemm_detail {
 

@@ -49,6 +49,13 @@ struct KArgs {
   int sk_units, sk_per_cta, sk_lcm;  // the planner keeps them below 2^31
   float* ws_partial;
   int* ws_count;
+  // Cluster split (dense, the kSplitCluster variant): tile t is computed by
+  // the cl_split CTAs of cluster t, CTA r of it taking K blocks
+  // [r * KB / cl_split, (r + 1) * KB / cl_split); the partial sums meet in
+  // shared memory (see cluster_reduce_store).
+  int cl_split;
+  // rows of A one TMA fill loads (a_box_rows(rows), see there)
+  int a_rows_box;
   // fused 1x128 quantization of the BF16 output (the kQ kernel variant)
   float* s_out;
   int64_t ld_s;
@@ -190,6 +197,15 @@ __device__ __forceinline__ void promote(float* acc, const uint32_t (&r)[W], floa
 
 // ---------------------------------------------------------------- host side
 inline int64_t ld4(int64_t r) { return (r + 3) / 4 * 4; }
+
+// Rows of A that one fill of a pipeline stage loads. A problem of one row
+// tile (fewer than BM rows, as in decoding) loads only its rows, rounded up
+// to the 8-row swizzle atom, instead of a full box whose rows past the end
+// the copy engine would fill with zeros: at 64 rows that is a quarter of
+// each stage's bytes. The MMA still runs 128 rows; the rows past the box
+// hold stale shared memory, which reaches only accumulator rows that are
+// never stored (row m of A B^T depends on row m of A alone).
+inline int a_box_rows(int64_t rows) { return rows < BM ? static_cast<int>((rows + 7) / 8 * 8) : BM; }
 
 // Tensor maps of one launch. Encoding them costs host time on every call,
 // and a map depends only on the pointers and sizes in the key, so launches

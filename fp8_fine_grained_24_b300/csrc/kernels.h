@@ -88,6 +88,9 @@ cudaError_t launch_gemm(const GemmProblem& p, uint32_t* status, uint64_t wait_li
 // (pair_gemm_eligible); launch_gemm dispatches to it.
 bool pair_gemm_eligible(const GemmProblem& p, int num_sms);
 void set_pair_gemm_enabled(bool on);
+// K split of decode-sized dense GEMMs: 0 automatic, 1 Stream-K only, 2 the
+// cluster split wherever it applies.
+void set_split_policy(int policy);
 cudaError_t launch_gemm_pair(const GemmProblem& p, uint32_t* status, uint64_t wait_limit_ns, int debug_skip_fill,
                              cudaStream_t stream, const char** detail);
 

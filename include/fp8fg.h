@@ -340,6 +340,12 @@ FP8FG_API int fp8fg_study_mma_accumulation(const uint8_t* A, const uint8_t* B, f
  *          SMs) to the CTA-pair kernel (tcgen05 cta_group::2, 256 x 256
  *          tiles); 0 (the default) keeps every GEMM on the single-CTA
  *          kernel. The environment variable FP8FG_PAIR=1 sets 1 at load.
+ *   key 4: how decode-sized dense GEMMs (128 x 128 output tiles at most
+ *          half the SMs) split K: 0 (the default) automatic, 1 Stream-K
+ *          over the caller's workspace only, 2 the cluster split (the CTAs
+ *          of a thread-block cluster share a tile and sum their partials
+ *          through distributed shared memory; no workspace) wherever it
+ *          applies. FP8FG_SPLIT=stream|cluster sets 1 or 2 at load.
  * Returns FP8FG_OK or FP8FG_ERR_INVALID_ARG.
  */
 FP8FG_API int fp8fg_debug_set(int key, int64_t value);

@@ -29,7 +29,7 @@ def _operands(M, N, K, seed):
     (256, 512, 384, torch.bfloat16),
     (200, 384, 1024, torch.bfloat16),   # ragged rows
     (130, 1024, 640, torch.float32),    # two row tiles, partial last one
-    (64, 2048, 1024, torch.bfloat16),   # decode-sized: K split over the SMs (Stream-K)
+    (64, 2048, 1024, torch.bfloat16),   # decode-sized: K split over the SMs
     (1024, 1024, 2048, torch.bfloat16), # several tiles per CTA
 ])
 def test_dgrad_matches_oracle(lib, M, N, K, out_dtype):
@@ -37,6 +37,21 @@ def test_dgrad_matches_oracle(lib, M, N, K, out_dtype):
     dx = lib.fp8_gemm_dgrad(qdy_d, sdy_d, qw_d, sw_d, out_dtype=out_dtype)
     lib.check()
     compare_gemm(dx, gemm.dgrad(qdy, sdy, qw, sw), out_dtype == torch.bfloat16)
+
+
+@pytest.mark.parametrize("policy", [1, 2])  # Stream-K, cluster split
+@pytest.mark.parametrize("M,N,K,out_dtype", [(64, 2048, 1024, torch.bfloat16), (96, 4096, 1152, torch.float32)])
+def test_dgrad_decode_split(lib, M, N, K, out_dtype, policy):
+    # W read MN-major with the reduction dimension split over the SMs
+    qdy, sdy, qw, sw, qdy_d, sdy_d, qw_d, sw_d = _operands(M, N, K, 6200 + M + K)
+    lib.set_split_policy(policy)
+    try:
+        outs = [lib.fp8_gemm_dgrad(qdy_d, sdy_d, qw_d, sw_d, out_dtype=out_dtype) for _ in range(2)]
+        lib.check()
+    finally:
+        lib.set_split_policy(lib.SPLIT_AUTO)
+    compare_gemm(outs[0], gemm.dgrad(qdy, sdy, qw, sw), out_dtype == torch.bfloat16)
+    assert torch.equal(outs[0], outs[1])
 
 
 def test_dgrad_fp32_accumulate(lib):

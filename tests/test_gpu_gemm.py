@@ -4,6 +4,8 @@ Operands are quantized by the oracle (never by the CUDA path) and uploaded;
 the library multiplies them; the oracle multiplies the same dequantized
 operands in FP64.
 """
+import contextlib
+
 import numpy as np
 import pytest
 import torch
@@ -453,7 +455,24 @@ def test_pair_kernel_timeout_reports_error_and_context_survives(lib):
 
 
 # ---------------------------------------------------------------- split-K (decode-sized M)
-def _split_case(fg, M, N, K, seed, out_dtype=torch.bfloat16, accumulate=False):
+# Decode-sized problems (128 x 128 tiles at most half the SMs) split K in
+# one of two ways, chosen by the split policy: Stream-K over the caller's
+# workspace, or the cluster split (the CTAs of a cluster share a tile and
+# sum their partials through distributed shared memory). Each split test
+# runs under both.
+SPLITS = pytest.mark.parametrize("policy", ["stream", "cluster"])
+
+
+@contextlib.contextmanager
+def split_policy(fg, policy):
+    fg.set_split_policy({"auto": fg.SPLIT_AUTO, "stream": fg.SPLIT_STREAM, "cluster": fg.SPLIT_CLUSTER}[policy])
+    try:
+        yield
+    finally:
+        fg.set_split_policy(fg.SPLIT_AUTO)
+
+
+def _split_case(fg, M, N, K, seed, out_dtype=torch.bfloat16, accumulate=False, policy="auto"):
     x = wl.activations(M, K, seed, device="cpu")
     w = wl.weights((N, K), seed + 1, device="cpu")
     qa, sa, qa_d, sa_d = _quant_a(x)
@@ -462,25 +481,51 @@ def _split_case(fg, M, N, K, seed, out_dtype=torch.bfloat16, accumulate=False):
     assert ws is not None, "expected a K-split for this shape"
     cref = gemm.gemm_dense(qa, sa, qb, sb)
     base = torch.randn((M, N), dtype=torch.float32, device="cuda") if accumulate else None
-    for _ in range(2):  # the workspace counters must come back to zero
-        c = base.clone() if accumulate else torch.empty((M, N), dtype=out_dtype, device="cuda")
-        fg.fp8_gemm_dense_out(qa_d, sa_d, qb_d, sb_d, c, accumulate=accumulate, workspace=ws)
-        torch.cuda.synchronize()
-        ref = cref + base.double().cpu().numpy() if accumulate else cref
-        compare_gemm(c, ref, out_dtype == torch.bfloat16)
+    outs = []
+    with split_policy(fg, policy):
+        for _ in range(2):  # the workspace counters must come back to zero
+            c = base.clone() if accumulate else torch.empty((M, N), dtype=out_dtype, device="cuda")
+            fg.fp8_gemm_dense_out(qa_d, sa_d, qb_d, sb_d, c, accumulate=accumulate, workspace=ws)
+            torch.cuda.synchronize()
+            ref = cref + base.double().cpu().numpy() if accumulate else cref
+            compare_gemm(c, ref, out_dtype == torch.bfloat16)
+            outs.append(c)
+    # partial sums are added in a fixed order whichever CTA finishes first
+    assert torch.equal(outs[0], outs[1]), "split result is not deterministic"
     return ws
 
 
+@SPLITS
 @pytest.mark.parametrize("M,N,K", [(1, 256, 2048), (64, 512, 4096), (130, 264, 2048), (128, 1024, 7168)])
-def test_split_k_matches_oracle(lib, M, N, K):
-    _split_case(lib, M, N, K, seed=M + N)
+def test_split_k_matches_oracle(lib, M, N, K, policy):
+    _split_case(lib, M, N, K, seed=M + N, policy=policy)
 
 
-def test_split_k_fp32_accumulate(lib):
-    _split_case(lib, 64, 520, 2048, seed=81, out_dtype=torch.float32, accumulate=True)
+@SPLITS
+def test_split_k_fp32_accumulate(lib, policy):
+    _split_case(lib, 64, 520, 2048, seed=81, out_dtype=torch.float32, accumulate=True, policy=policy)
 
 
-def test_split_k_small_workspace_falls_back(lib):
+# Cluster split sizes: S = min(8, SMs // tiles, K blocks // 4), lowered
+# until every tile's cluster is resident at once. On 148 SMs these shapes
+# ask for S = 8 (one tile), 4, 3, 5, 6 and 7, then 2 with a ragged last
+# column tile (N = 3144 and 6344: the last tile has 72 columns), once with
+# a second row tile of 2 rows (M = 130). S that does not divide the 16
+# column chunks of a tile gives CTAs unequal shares (S = 3: 5, 5, 6).
+@pytest.mark.parametrize("M,N,K", [(64, 128, 4096), (64, 3072, 2048), (64, 5760, 2048), (32, 3712, 2560),
+                                   (64, 3072, 3072), (16, 2688, 3584), (130, 3144, 1024), (64, 6344, 1024)])
+def test_cluster_split_sizes(lib, M, N, K):
+    _split_case(lib, M, N, K, seed=M + N + K, policy="cluster")
+
+
+def test_cluster_split_fp32_accumulate_ragged(lib):
+    _split_case(lib, 130, 264, 4096, seed=85, out_dtype=torch.float32, accumulate=True, policy="cluster")
+
+
+@SPLITS
+def test_split_k_small_workspace_falls_back(lib, policy):
+    # a workspace too small for Stream-K: the GEMM runs unsplit (Stream-K
+    # policy) or on the cluster split, and the workspace is never written
     M, N, K = 64, 512, 2048
     x = wl.activations(M, K, 82, device="cpu")
     w = wl.weights((N, K), 83, device="cpu")
@@ -488,32 +533,41 @@ def test_split_k_small_workspace_falls_back(lib):
     qb, sb, qb_d, sb_d = _quant_b(w)
     small = torch.zeros(64, dtype=torch.uint8, device="cuda")
     c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    lib.fp8_gemm_dense_out(qa_d, sa_d, qb_d, sb_d, c, workspace=small)
+    with split_policy(lib, policy):
+        lib.fp8_gemm_dense_out(qa_d, sa_d, qb_d, sb_d, c, workspace=small)
     compare_gemm(c, gemm.gemm_dense(qa, sa, qb, sb), True)
     assert torch.count_nonzero(small) == 0
 
 
-def test_split_k_wgrad_row_scales(lib):
+@SPLITS
+def test_split_k_wgrad_row_scales(lib, policy):
     # weight gradient with many tokens and a small output: K (tokens) is split
     T, N, C = 2048, 136, 264
     qgT, sgT, qxT, sxT = _wgrad_operands(T, N, C, 84)
     ws = lib.gemm_workspace(N, C, T)
     assert ws is not None
-    out = torch.empty((N, C), dtype=torch.float32, device="cuda")
-    lib.fp8_gemm_dense_out(dev(qgT), dev(pad_rows_scale(sgT, N)), dev(qxT), dev(pad_rows_scale(sxT, C)), out,
-                           b_scale_kind=lib.SCALE_ROW, workspace=ws)
-    compare_gemm(out, gemm.wgrad(qgT, sgT, qxT, sxT), False)
+    outs = []
+    with split_policy(lib, policy):
+        for _ in range(2):
+            out = torch.empty((N, C), dtype=torch.float32, device="cuda")
+            lib.fp8_gemm_dense_out(dev(qgT), dev(pad_rows_scale(sgT, N)), dev(qxT), dev(pad_rows_scale(sxT, C)), out,
+                                   b_scale_kind=lib.SCALE_ROW, workspace=ws)
+            compare_gemm(out, gemm.wgrad(qgT, sgT, qxT, sxT), False)
+            outs.append(out)
+    assert torch.equal(outs[0], outs[1])
 
 
 @pytest.mark.slow
+@SPLITS
 @pytest.mark.parametrize("M,N,K", wl.DECODE_CASES)
-def test_decode_full_sampled(lib, M, N, K):
+def test_decode_full_sampled(lib, M, N, K, policy):
     x = wl.activations(M, K, 1003, device="cuda")
     w = wl.weights((N, K), 1004 + N, device="cuda")
     qa_d, sa_d = lib.fp8_quant_1x128(x)
     qb_d, sb_d = lib.fp8_quant_128x128(w)
-    c = lib.fp8_gemm_dense(qa_d, sa_d, qb_d, sb_d)
-    torch.cuda.synchronize()
+    with split_policy(lib, policy):
+        c = lib.fp8_gemm_dense(qa_d, sa_d, qb_d, sb_d)
+        torch.cuda.synchronize()
     qa, sa = quant.quant_1x128(to_np32(x))
     for nb in (0, 13, N // 128 - 1):
         cols = slice(nb * 128, nb * 128 + 128)
@@ -528,7 +582,7 @@ def test_decode_full_sampled(lib, M, N, K):
 # pieces come from several CTAs; the last piece to arrive sums them in
 # order. On 148 SMs, M=64, N=1792, K=6912 gives 7 tiles of 54 K blocks,
 # U = 5.
-def _sk_case(fg, M, N, K, seed, out_dtype=torch.bfloat16, accumulate=False, rows=None):
+def _sk_case(fg, M, N, K, seed, out_dtype=torch.bfloat16, accumulate=False, rows=None, policy="stream"):
     x = wl.activations(M, K, seed, device="cpu")
     w = wl.weights((N, K), seed + 1, device="cpu")
     qa, sa, qa_d, sa_d = _quant_a(x)
@@ -540,17 +594,19 @@ def _sk_case(fg, M, N, K, seed, out_dtype=torch.bfloat16, accumulate=False, rows
     cref = gemm.gemm_dense(qa, sa, qb, sb, rows=sel)
     base = torch.randn((M, N), dtype=torch.float32, device="cuda") if accumulate else None
     outs = []
-    for _ in range(2):  # the arrival counters must come back to zero
-        c = base.clone() if accumulate else torch.empty((M, N), dtype=out_dtype, device="cuda")
-        fg.fp8_gemm_dense_out(qa_d, sa_d, qb_d, sb_d, c, accumulate=accumulate, workspace=ws)
-        torch.cuda.synchronize()
-        ref = cref + base.double().cpu().numpy()[sel] if accumulate else cref
-        compare_gemm(c[torch.as_tensor(sel, device="cuda")], ref, out_dtype == torch.bfloat16)
-        outs.append(c)
-    assert torch.equal(outs[0], outs[1]), "Stream-K result is not deterministic"
-    # the unsplit product agrees within the same tolerance
+    with split_policy(fg, policy):
+        for _ in range(2):  # the arrival counters must come back to zero
+            c = base.clone() if accumulate else torch.empty((M, N), dtype=out_dtype, device="cuda")
+            fg.fp8_gemm_dense_out(qa_d, sa_d, qb_d, sb_d, c, accumulate=accumulate, workspace=ws)
+            torch.cuda.synchronize()
+            ref = cref + base.double().cpu().numpy()[sel] if accumulate else cref
+            compare_gemm(c[torch.as_tensor(sel, device="cuda")], ref, out_dtype == torch.bfloat16)
+            outs.append(c)
+    assert torch.equal(outs[0], outs[1]), "split result is not deterministic"
+    # the unsplit product (Stream-K policy, no workspace) agrees within the same tolerance
     c = base.clone() if accumulate else torch.empty((M, N), dtype=out_dtype, device="cuda")
-    fg.fp8_gemm_dense_out(qa_d, sa_d, qb_d, sb_d, c, accumulate=accumulate, workspace=None)
+    with split_policy(fg, "stream"):
+        fg.fp8_gemm_dense_out(qa_d, sa_d, qb_d, sb_d, c, accumulate=accumulate, workspace=None)
     torch.cuda.synchronize()
     compare_gemm(c[torch.as_tensor(sel, device="cuda")], ref, out_dtype == torch.bfloat16)
 

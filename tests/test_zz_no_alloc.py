@@ -7,7 +7,9 @@ inside the library instead. These tests call it through the C ABI and check
 its output against the oracle's FP64 product of the same (oracle-quantized)
 operands, within the GEMM tolerance the other GPU tests use, on two calls in
 a row (the shared scratch must be left usable by the first call). Shapes that
-split K are asserted to need scratch, so the static array is really used.
+split K are asserted to need scratch and run under both split policies:
+Stream-K, which sums its partials in the static array, and the cluster
+split, which needs none.
 The file sorts last so that a run stopping at the first failure has already
 run every other test.
 """
@@ -50,13 +52,20 @@ def _operands(M, N, K, seed, col_blocks):
     return dev(qa), dev(pad_rows_scale(sa, M)), dev(qb), dev(sb), refs
 
 
+@pytest.fixture(params=["stream", "cluster"])
+def policy(request, lib):
+    lib.set_split_policy(lib.SPLIT_STREAM if request.param == "stream" else lib.SPLIT_CLUSTER)
+    yield request.param
+    lib.set_split_policy(lib.SPLIT_AUTO)
+
+
 @pytest.mark.parametrize("M,N,K,out_dtype,splits", [
-    (64, 4096, 7168, torch.bfloat16, True),    # splits K: uses the static scratch
+    (64, 4096, 7168, torch.bfloat16, True),    # splits K: Stream-K uses the static scratch
     (128, 7168, 2048, torch.bfloat16, True),   # splits K
     (64, 520, 2048, torch.float32, True),      # splits K, FP32 output
     (1024, 4096, 512, torch.bfloat16, False),  # 128 tiles fill the GPU: no split, no scratch
 ])
-def test_noalloc_matches_oracle(lib, M, N, K, out_dtype, splits):
+def test_noalloc_matches_oracle(lib, M, N, K, out_dtype, splits, policy):
     fg = lib
     f = _entry(fg)
     need = fg.gemm_workspace_size(M, N, K)
@@ -75,9 +84,10 @@ def test_noalloc_matches_oracle(lib, M, N, K, out_dtype, splits):
             compare_gemm(c[:, nb * 128:min(N, nb * 128 + 128)], ref, out_dtype == torch.bfloat16)
 
 
-def test_noalloc_fp32_accumulate_matches_oracle(lib):
-    # C += A B^T into a nonzero FP32 C: with K split, the last piece of each
-    # tile adds the summed partials into C
+def test_noalloc_fp32_accumulate_matches_oracle(lib, policy):
+    # C += A B^T into a nonzero FP32 C: with K split, the partials' sum is
+    # added into C once (by the last Stream-K piece of each tile, or by the
+    # cluster's reduction)
     fg = lib
     f = _entry(fg)
     M, N, K = 64, 1792, 6912
