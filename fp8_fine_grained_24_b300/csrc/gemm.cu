@@ -308,74 +308,100 @@ __device__ __forceinline__ bool sk_reduce(const KArgs& a, const Tile& ti, int ro
 }
 
 // Cluster split. The tile's 16 column chunks of 8 are divided among the S
-// CTAs of its cluster, CTA r owning chunks [b(r), b(r+1)), b(r) =
-// floor(16 r / S). Once every CTA of the cluster is past its K loop (a
-// cluster barrier: from then on no stage of any of them is in use), each
-// epilogue thread stores its row's FP32 partial sums, chunk by chunk, into
-// the shared memory of the chunk's owner, in the slot of the sending rank:
-// slot q holds BM rows of kPitch(S) floats. After a second barrier (release
-// and acquire: the stores have landed) every CTA sums its own chunks over
-// the S slots in rank order, so the result does not depend on timing, and
-// stores them. Nothing reads another CTA's shared memory after that
-// barrier, so a CTA may then leave.
-// kPitch: the owner's widest share, plus 4 floats that make the row pitch
-// an odd number of 16-byte units, so that a warp's 32 rows land on
-// distinct bank groups.
-template <int BN>
+// CTAs of its cluster, CTA r owning chunks [first(r), first(r + 1)),
+// first(r) = floor(16 r / S). Each epilogue warp first writes its 32 rows
+// x NC columns of FP32 partial sums into its own transpose area in this
+// CTA's shared memory (the pipeline stages are idle once its K loop is
+// done). Once every CTA of the cluster is past its K loop (a cluster
+// barrier: from then on no stage of any of them is in use), the warp reads
+// them back so that its lanes cover consecutive 16-byte pieces of an
+// owner's rows, and stores them with st.shared::cluster into slot `rank` of
+// the owner's receive area: one warp-wide store moves up to 512 contiguous
+// bytes, where storing each lane's own row would scatter 32 pieces. After a
+// second barrier (release and acquire: the stores have landed) every CTA
+// sums its chunks over the S slots in rank order, so the result does not
+// depend on timing, and stores them. Nothing reads another CTA's shared
+// memory after that barrier, so a CTA may then leave.
+// A transpose row is NC floats plus 16 bytes (an odd number of 16-byte
+// units, so that the lanes' rows fall on distinct bank groups); a receive
+// row is the widest share, ceil(16 / S) chunks.
+constexpr int kMaxClusterSplit = 8;  // portable cluster size
+
+template <int BN, int NC, int kEpiWarps>
 struct ClusterPart {
   static constexpr int kChunks = BN / 8;
-  static constexpr int kMaxSplit = 8;  // portable cluster size
-  static __host__ __device__ constexpr int pitch(int S) { return (kChunks + S - 1) / S * 8 + 4; }
-  static __host__ __device__ constexpr int bytes(int S) { return S * BM * pitch(S) * 4; }
-  static constexpr int max_bytes(int S = 2) {
-    return S > kMaxSplit ? 0 : (bytes(S) > max_bytes(S + 1) ? bytes(S) : max_bytes(S + 1));
+  static constexpr int kChunkBytes = 32;
+  static constexpr int kMaxSplit = kMaxClusterSplit;
+  static constexpr int kXposePitch = NC * 4 + 16;
+  static constexpr int kXposeBytes = kEpiWarps * 32 * kXposePitch;
+  static constexpr int kRecvOff = (kXposeBytes + 1023) / 1024 * 1024;
+  static __host__ __device__ constexpr int recv_pitch(int S) { return (kChunks + S - 1) / S * kChunkBytes; }
+  static constexpr int max_recv_bytes(int S = 2) {
+    return S > kMaxSplit ? 0
+                         : (S * BM * recv_pitch(S) > max_recv_bytes(S + 1) ? S * BM * recv_pitch(S)
+                                                                            : max_recv_bytes(S + 1));
   }
-  // the owner of chunk ch: the r with b(r) <= ch < b(r + 1)
+  static constexpr int kBytes = kRecvOff + max_recv_bytes();
+  static __host__ __device__ constexpr int first(int r, int S) { return r * kChunks / S; }
+  // the owner of chunk ch: the r with first(r) <= ch < first(r + 1)
   static __device__ __forceinline__ int owner(int ch, int S) { return (ch * S + S - 1) / kChunks; }
-  static __device__ __forceinline__ int first(int r, int S) { return r * kChunks / S; }
 };
 
-// One epilogue thread's row of partial sums (columns col0 .. col0 + NC of
-// the tile) to the chunks' owners.
-template <int BN, int NC>
-__device__ __forceinline__ void cluster_push(const KArgs& a, const Tile& ti, int row_in_tile, int col0,
-                                             uint32_t sbase, const float (&acc)[NC]) {
-  using P = ClusterPart<BN>;
-  if (ti.m0 + row_in_tile >= a.rows) return;  // rows past the end are never stored
+// One epilogue warp's partial sums (rows row_base .. row_base + 31 of the
+// tile, one per lane, columns col0 .. col0 + NC) into its transpose area.
+template <class P, int NC>
+__device__ __forceinline__ void cluster_stage(uint8_t* xpose, int lane, const float (&acc)[NC]) {
+  float4* d = reinterpret_cast<float4*>(xpose + lane * P::kXposePitch);
+#pragma unroll
+  for (int j = 0; j < NC / 4; ++j) d[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+}
+
+// The warp's staged rows, owner by owner, into the owners' receive areas.
+template <class P, int NC>
+__device__ __forceinline__ void cluster_push(const KArgs& a, const Tile& ti, int row_base, int col0, int lane,
+                                             const uint8_t* xpose, uint32_t sbase) {
   const int S = a.cl_split;
   const int me = static_cast<int>(cluster_ctarank());
-  const int pitch = P::pitch(S);
-#pragma unroll
-  for (int k = 0; k < NC / 8; ++k) {
-    const int ch = col0 / 8 + k;
-    const int r = P::owner(ch, S);
-    const int lc = ch - P::first(r, S);
-    const uint32_t dst = map_to_cta(sbase, static_cast<uint32_t>(r)) +
-                         static_cast<uint32_t>(((me * BM + row_in_tile) * pitch + lc * 8) * 4);
-    st_cluster_f4(dst, acc[8 * k], acc[8 * k + 1], acc[8 * k + 2], acc[8 * k + 3]);
-    st_cluster_f4(dst + 16, acc[8 * k + 4], acc[8 * k + 5], acc[8 * k + 6], acc[8 * k + 7]);
+  const int valid = a.rows - (ti.m0 + row_base) < 32 ? a.rows - (ti.m0 + row_base) : 32;
+  const int c0 = col0 / 8;
+  const int pitch = P::recv_pitch(S);
+  for (int r = P::owner(c0, S); r <= P::owner(c0 + NC / 8 - 1, S); ++r) {
+    const int k_lo = c0 > P::first(r, S) ? c0 : P::first(r, S);
+    const int k_hi = c0 + NC / 8 < P::first(r + 1, S) ? c0 + NC / 8 : P::first(r + 1, S);
+    const int per_row = 2 * (k_hi - k_lo);  // 16-byte pieces of one row for this owner
+    // p / per_row by multiplication (exact for p * per_row < 2^16)
+    const uint32_t inv = (65536u + static_cast<uint32_t>(per_row) - 1) / static_cast<uint32_t>(per_row);
+    const uint32_t dst = map_to_cta(sbase + P::kRecvOff, static_cast<uint32_t>(r)) +
+                         static_cast<uint32_t>((me * BM + row_base) * pitch + (k_lo - P::first(r, S)) * P::kChunkBytes);
+    const uint8_t* src = xpose + (k_lo - c0) * P::kChunkBytes;
+    for (int p = lane; p < valid * per_row; p += 32) {
+      const int row = static_cast<int>((static_cast<uint32_t>(p) * inv) >> 16);
+      const int pc = p - row * per_row;
+      const float4 v = *reinterpret_cast<const float4*>(src + row * P::kXposePitch + pc * 16);
+      st_cluster_f4(dst + static_cast<uint32_t>(row * pitch + pc * 16), v.x, v.y, v.z, v.w);
+    }
   }
 }
 
-// This CTA's chunks of the tile: the sum over the S slots, stored to C.
-template <int BN, bool kF32>
-__device__ __forceinline__ void cluster_reduce_store(const KArgs& a, const Tile& ti, const float* part) {
-  using P = ClusterPart<BN>;
+// This CTA's chunks of the tile: the sum over the S slots of its receive
+// area, stored to C.
+template <class P, bool kF32>
+__device__ __forceinline__ void cluster_reduce_store(const KArgs& a, const Tile& ti, const uint8_t* recv) {
   const int S = a.cl_split;
   const int r = static_cast<int>(cluster_ctarank());
   const int c_begin = P::first(r, S), nch = P::first(r + 1, S) - c_begin;
-  const int pitch = P::pitch(S);
+  const int pitch = P::recv_pitch(S);
   const int rows = a.rows - ti.m0 < BM ? a.rows - ti.m0 : BM;
   for (int i = threadIdx.x; i < rows * nch; i += blockDim.x) {
     const int row = i / nch;
     const int lc = i - row * nch;
     const int col = ti.n0 + (c_begin + lc) * 8;
     if (col >= a.N) continue;  // N % 8 == 0: a chunk is wholly inside or outside
-    const float* src = part + row * pitch + lc * 8;
+    const uint8_t* src = recv + row * pitch + lc * P::kChunkBytes;
     float4 lo = make_float4(0.0f, 0.0f, 0.0f, 0.0f), hi = lo;
     for (int q = 0; q < S; ++q) {
       const float4 x = *reinterpret_cast<const float4*>(src + q * BM * pitch);
-      const float4 y = *reinterpret_cast<const float4*>(src + q * BM * pitch + 4);
+      const float4 y = *reinterpret_cast<const float4*>(src + q * BM * pitch + 16);
       lo.x += x.x; lo.y += x.y; lo.z += x.z; lo.w += x.w;
       hi.x += y.x; hi.y += y.y; hi.z += y.z; hi.w += y.w;
     }
@@ -471,8 +497,9 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   static_assert(kSplit != kSplitCluster || (BN == 128 && !kQ && !kCompact),
                 "cluster split: 128-column tiles, row-by-row stores, dense layout");
   using C = Cfg<BN>;
-  static_assert(kSplit != kSplitCluster || ClusterPart<BN>::max_bytes() <= C::kOffEpi,
-                "the partial tiles fit in the pipeline stages");
+  using CP = ClusterPart<BN, C::kColsPerWarp, C::kEpiWarps>;
+  static_assert(kSplit != kSplitCluster || CP::kBytes <= C::kOffEpi,
+                "the transpose and receive areas fit in the pipeline stages");
   constexpr int S = C::kStages;
   constexpr int NB = C::kAccBufs;
   extern __shared__ uint8_t smem_raw[];
@@ -695,13 +722,18 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         // a Stream-K piece of a split tile: only the last to arrive stores
         if (ti.kbc != a.KB) store = sk_reduce<NC, C::kEpiWarps>(a, ti, row_in_tile, ew, lane, acc);
       } else if constexpr (kSplit == kSplitCluster) {
-        // first cluster barrier: every CTA of the cluster is past its K
-        // loop (its MMAs complete, its fills landed), so the partials may
-        // go into the owners' stages
+        // this warp's partial into its transpose area (its own stages are
+        // free: every MMA has completed and every fill has landed, the
+        // fence orders the tensor core's reads of them before these
+        // writes); then the first cluster barrier: every CTA of the cluster
+        // is past its K loop, so the owners' receive areas are free too
+        uint8_t* xpose = smem + ew * 32 * CP::kXposePitch;
         fence_async_shared();
+        cluster_stage<CP, NC>(xpose, lane, acc);
+        __syncwarp();
         cluster_sync();
         pushed = true;
-        cluster_push<BN, NC>(a, ti, row_in_tile, col0, sbase, acc);
+        cluster_push<CP, NC>(a, ti, quarter * 32, col0, lane, xpose, sbase);
         store = false;
       }
       bool staged = false;
@@ -764,8 +796,8 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       cluster_sync();
     }
     cluster_sync();
-    cluster_reduce_store<BN, kF32>(a, decode_tile<BN>(a, static_cast<int>(blockIdx.x / a.cl_split)),
-                                   reinterpret_cast<const float*>(smem));
+    cluster_reduce_store<CP, kF32>(a, decode_tile<BN>(a, static_cast<int>(blockIdx.x / a.cl_split)),
+                                   smem + CP::kRecvOff);
   }
   __syncthreads();
   if (warp == 1) {
@@ -889,7 +921,7 @@ int split_policy() { return g_split_policy.load(std::memory_order_relaxed); }
 // threads and shared memory, so one query serves them all).
 template <class Fn>
 cudaError_t cluster_capacity(Fn fn, int size, int* fit) {
-  static std::atomic<int> cache[64][ClusterPart<128>::kMaxSplit + 1];
+  static std::atomic<int> cache[64][kMaxClusterSplit + 1];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -931,7 +963,7 @@ cudaError_t pick_cluster_split(int mode, int64_t rows, int64_t N, int64_t K, int
   const int64_t tiles = ((rows + BM - 1) / BM) * ((N + 127) / 128);
   if (tiles <= 0 || tiles * 2 > num_sms) return cudaSuccess;
   int64_t S = num_sms / tiles;
-  if (S > ClusterPart<128>::kMaxSplit) S = ClusterPart<128>::kMaxSplit;
+  if (S > kMaxClusterSplit) S = kMaxClusterSplit;
   if (S > KB / kMinUnits) S = KB / kMinUnits;
   for (; S >= 2; --S) {
     int fit = 0;
@@ -1132,13 +1164,24 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
       return e;
     }
   }
-  if (cl >= 2 && (policy == kPolicyCluster || policy == kPolicyAuto)) {
+  // Automatic: the cluster split where it saves each CTA at least
+  // kMinSavedBlocks K blocks (its reduction costs about that much: ~3 us
+  // against ~0.33 us per 128-K block of the K loop, measured), whole tiles
+  // where it applies but saves less (Stream-K's reduction costs more), and
+  // Stream-K only where the cluster split does not apply.
+  constexpr int64_t kMinSavedBlocks = 10;
+  const bool cluster_pays = cl >= 2 && KB - (KB + cl - 1) / cl >= kMinSavedBlocks;
+  const bool use_cluster = cl >= 2 && (policy == kPolicyCluster || (policy == kPolicyAuto && cluster_pays));
+  const bool use_stream_k = plan.sk && !use_cluster && !(policy == kPolicyAuto && cl >= 2);
+  if (use_cluster) {
     a.cl_split = cl;
     e = launch_kernel_cluster(kernels[3], dim3(static_cast<unsigned>(a.num_tiles * cl)), dim3(C::kThreads), C::kSmem,
                               stream, static_cast<unsigned>(cl), tmA, tmB, tmSA, tmSB, tmC, tmQ, a);
-  } else if (!plan.sk) {
-    e = launch_kernel(kernels[masked ? 2 : 0], dim3(plan.grid), dim3(C::kThreads), C::kSmem, stream, tmA, tmB, tmSA,
-                      tmSB, tmC, tmQ, a);
+  } else if (!use_stream_k) {
+    // whole tiles: one persistent CTA per SM at most
+    const int grid = a.num_tiles < num_sms ? a.num_tiles : num_sms;
+    e = launch_kernel(kernels[masked ? 2 : 0], dim3(grid), dim3(C::kThreads), C::kSmem, stream, tmA, tmB, tmSA, tmSB,
+                      tmC, tmQ, a);
   } else {
     a.dp_tiles = plan.dp_tiles;
     a.sk_tile0 = plan.dp_tiles;
