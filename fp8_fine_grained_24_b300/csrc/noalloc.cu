@@ -1,8 +1,10 @@
 // fp8_gemm_dense_noalloc: the dense FP8 GEMM for callers that cannot
 // allocate device memory.
 //
-// fp8_gemm_dense asks its caller for a scratch buffer when it splits K for
-// decode-sized problems. Some callers have no way to provide one: a plug-in
+// fp8_gemm_dense asks its caller for a scratch buffer for decode-sized
+// problems, which its Stream-K split sums partial tiles in (its cluster
+// split, the default where it applies, needs none). Some callers have no
+// way to provide one: a plug-in
 // or operator library that is handed device pointers by a host application
 // which owns every byte of device memory and exposes no allocator; code on a
 // latency-critical loop where a device allocation (which can synchronize the

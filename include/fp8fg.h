@@ -150,18 +150,22 @@ FP8FG_API int fp8_requant_128x1(const void* src, int src_dtype, const float* s_s
  *   C          [M][N] of out_dtype (BF16 or FP32), written
  *   accumulate 1: C += result (FP32 output only: weight-gradient
  *              accumulation); 0: C = result
- *   workspace  device scratch for splitting tiles along K over several SMs
- *              (Stream-K), used when the output has too few tiles to occupy
- *              the GPU (at most half as many as SMs: decode-sized M).
- *              fp8fg_gemm_workspace_size(M, N, K) bytes, 16-byte aligned,
- *              zero-filled before its first use; every call leaves its
- *              counters zero-filled again (re-zero the workspace after a call
- *              that reported FP8FG_ERR_TIMEOUT). Calls that share a workspace
- *              must not overlap on the GPU. NULL, or fewer bytes than that
- *              size, runs the same product without splitting K. Split tiles
- *              are summed in a fixed order: results are deterministic for a
- *              given shape and SM count, and differ from the unsplit run by
- *              FP32 rounding only.
+ *   workspace  device scratch for one of the two ways of splitting K when
+ *              the output has too few tiles to occupy the GPU (at most half
+ *              as many 128x128 tiles as SMs: decode-sized M). The default
+ *              split runs each tile on the CTAs of a thread-block cluster,
+ *              which sum their partials through distributed shared memory
+ *              and need no workspace; Stream-K (chosen where the cluster
+ *              split does not apply, or by fp8fg_debug_set key 4) sums them
+ *              in the workspace. fp8fg_gemm_workspace_size(M, N, K) bytes,
+ *              16-byte aligned, zero-filled before its first use; every call
+ *              leaves its counters zero-filled again (re-zero the workspace
+ *              after a call that reported FP8FG_ERR_TIMEOUT). Calls that
+ *              share a workspace must not overlap on the GPU. NULL, or fewer
+ *              bytes than that size, runs without Stream-K. Split tiles are
+ *              summed in a fixed order: results are deterministic for a
+ *              given shape, SM count and split policy, and differ from the
+ *              unsplit run by FP32 rounding only.
  * Requires K % 128 == 0, N % 8 == 0, 16-byte aligned A, B, C.
  */
 FP8FG_API int fp8_gemm_dense(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
