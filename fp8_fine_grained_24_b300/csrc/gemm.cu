@@ -62,7 +62,15 @@ struct Cfg {
   // 256 x kRegsHigh must not exceed that (checked on the host against the
   // compiled register count before the first launch).
   static constexpr bool kRegSplit = (BN == 256);
-  static constexpr int kEpiWarp0 = kRegSplit ? 4 : 2;        // first promotion warp
+  // MMA issuers: each tcgen05.mma costs its issuing thread a fixed ~50 ns
+  // on top of the tensor core's work (measured: splitting a block's 4 MMAs
+  // into 8 half-width ones adds ~23 ns per extra instruction), so with one
+  // issuer a 128-wide block takes ~330 ns where the tensor core needs ~135.
+  // A second issuer warp takes every other K block (its own TMEM buffer and
+  // stage, its own commits). BN=256 uses warp 2, idle otherwise; BN=128 adds
+  // a warp; BN=192 keeps one.
+  static constexpr int kMaxIssuers = (BN == 192) ? 1 : 2;
+  static constexpr int kEpiWarp0 = kRegSplit ? 4 : (BN == 128 ? 3 : 2);  // first promotion warp
   static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
   static constexpr int kRegsLaunch = 168, kRegsLow = 48, kRegsHigh = 224;
   static_assert(!kRegSplit || (kEpiWarps == 8 && 128 * kRegsLow + 256 * kRegsHigh <= kThreads * kRegsLaunch),
@@ -535,7 +543,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       mbar_init(tfull_bar(b), 1);
       mbar_init(tempty_bar(b), C::kEpiWarps);
     }
-    mbar_init(drain_bar, 1);
+    mbar_init(drain_bar, static_cast<uint32_t>(a.mma_issuers));
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
@@ -587,9 +595,13 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         mbar_wait(full_bar(i % S), (i / S) & 1, nullptr, 0, a.wait_limit_ns);
       }
     }
-   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+   } else if (warp == 1 || (C::kMaxIssuers > 1 && warp == 2)) {
+    // ------------------------------------------------------------ MMA issuers
+    // issuer i of a.mma_issuers (1 or 2) takes the K blocks it with
+    // it % a.mma_issuers == i
+    const uint32_t issuer = static_cast<uint32_t>(warp - 1);
+    const uint32_t nis = static_cast<uint32_t>(a.mma_issuers);
+    if (lane == 0 && issuer < nis) {
       constexpr uint32_t idesc = f8_idesc(BM, BN, kBT);
       uint32_t it = 0;
       bool ok = true;
@@ -598,6 +610,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       while (ok && work_next<BN, kSplit, kCompact>(a, wk, ti)) {
         if (ti.skip) continue;
         for (int kb = ti.kb0; kb < ti.kb0 + ti.kbc; ++kb, ++it) {
+          if ((it & (nis - 1)) != issuer) continue;  // the other issuer's block
           const uint32_t s = it % S, ph = (it / S) & 1;
           const uint32_t buf = it % NB, tph = (it / NB) & 1;
           if (!mbar_wait(tempty_bar(buf), tph ^ 1, a.status, kStatusTimeoutMma, a.wait_limit_ns) ||
@@ -621,7 +634,8 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
           mma_commit(tfull_bar(buf));
         }
       }
-      // All MMAs issued by this thread complete before TMEM is released.
+      // All MMAs issued by the issuers complete before TMEM is released
+      // (the drain barrier counts one commit per issuer).
       mma_commit(drain_bar);
       if (!mbar_wait(drain_bar, 0, nullptr, 0, a.wait_limit_ns)) atomicCAS(a.status, 0u, kStatusTimeoutDrain);
     }
@@ -916,6 +930,16 @@ std::atomic<int> g_split_policy{[] {
 
 int split_policy() { return g_split_policy.load(std::memory_order_relaxed); }
 
+// Two MMA issuers where the tile configuration has room for them
+// (FP8FG_ISSUERS=1 keeps one, for timing comparisons).
+bool two_issuers_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("FP8FG_ISSUERS");
+    return !(v && v[0] == '1');
+  }();
+  return on;
+}
+
 // Clusters of `size` CTAs of `fn` that fit on the device at once (cached per
 // device and size; the kernels that share a tile configuration have the same
 // threads and shared memory, so one query serves them all).
@@ -1079,6 +1103,7 @@ cudaError_t launch_bn(const GemmProblem& p, uint32_t* status, uint64_t wait_limi
   a.ws_partial = nullptr;
   a.ws_count = nullptr;
   a.cl_split = 0;
+  a.mma_issuers = (C::kMaxIssuers > 1 && two_issuers_enabled()) ? 2 : 1;
   a.a_rows_box = a_box_rows(p.rows);
   a.s_out = p.s_out;
   a.ld_s = ld4(p.rows);

@@ -56,6 +56,8 @@ struct KArgs {
   int cl_split;
   // rows of A one TMA fill loads (a_box_rows(rows), see there)
   int a_rows_box;
+  // MMA issuer warps (1 or 2): issuer i takes the K blocks it % n == i
+  int mma_issuers;
   // fused 1x128 quantization of the BF16 output (the kQ kernel variant)
   float* s_out;
   int64_t ld_s;
