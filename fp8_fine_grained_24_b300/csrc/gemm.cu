@@ -11,15 +11,17 @@
 //               128-byte swizzle), the 128 row scales of A and, for per-row
 //               B scales, BN column scales, into an S-stage shared-memory
 //               ring guarded by full/empty mbarriers;
-//   warp 1      MMA issuer: 4 x tcgen05.mma.kind::f8f6f4 (K=32 each) per
-//               128-K block into one of several TMEM accumulator buffers,
-//               fresh per K block (no accumulation across blocks), then
-//               commits to the stage's "empty" and the buffer's "full"
-//               barriers;
-//   warps 2..   promotion + epilogue: tcgen05.ld the K block's FP32 partial
+//   warps 1, 2  MMA issuers, alternate K blocks: 4 x
+//               tcgen05.mma.kind::f8f6f4 (K=32 each) per 128-K block into
+//               one of several TMEM accumulator buffers, fresh per K block
+//               (no accumulation across blocks), then a commit to the
+//               buffer's "full" barrier (two issuers, because each MMA
+//               costs its issuing thread a fixed time);
+//   the rest    promotion + epilogue: tcgen05.ld the K block's FP32 partial
 //               sums, acc += (sA[m,kb] * sB[n,kb]) * partial in registers,
-//               release the TMEM buffer; after the last K block convert and
-//               store the tile (BF16 or FP32, optional C += for FP32).
+//               release the TMEM buffer and the stage (whose scales they
+//               read); after the last K block convert and store the tile
+//               (BF16 or FP32, optional C += for FP32).
 // Thread <-> data: each epilogue thread owns one row of the tile (its TMEM
 // lane) and a contiguous group of columns, so the A scale is one scalar per
 // thread per K block and the B block scale one scalar per warp.
