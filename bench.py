@@ -55,9 +55,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # reported traffic is null. Writes sit below M*N*2 because output lines still
 # in L2 when the kernel ends are written back after it.
 NCU_TRAFFIC = {
-    "kernel_sha": "a9c9633b509f2288",
-    "per_launch": {2112: 45539072 + 452864, 24576: 214712576 + 179256320,
-                   7168: 83838464 + 36464384, 4096: 60808448 + 11978752},
+    "kernel_sha": "05c61eeb057f46d2",
+    "per_launch": {2112: 45537536 + 681216, 24576: 212200960 + 180371200,
+                   7168: 83592192 + 37598208, 4096: 60659968 + 11886592},
 }
 
 
