@@ -88,3 +88,8 @@ def test_host_validation_without_gpu():
     assert L.fp8_gemm_grouped_masked(*args, 0, None, 0, good, fg.BF16, 0, 2, 128, 128, 128, 0, None) == \
         fg.ERR_INVALID_ARG
     assert L.fp8fg_debug_set(99, 0) == fg.ERR_INVALID_ARG
+    # split policy (key 4): 0 automatic, 1 Stream-K, 2 cluster split; others rejected
+    for bad in (-1, 3):
+        assert L.fp8fg_debug_set(4, bad) == fg.ERR_INVALID_ARG
+    for v in (fg.SPLIT_STREAM, fg.SPLIT_CLUSTER, fg.SPLIT_AUTO):
+        assert L.fp8fg_debug_set(4, v) == fg.OK
