@@ -62,18 +62,22 @@ struct Walk {
   int64_t s2;
   int s1, s0;
 
+  // Chunk indices, steps and r1 * r0 are below 2^31 (the launchers check
+  // the chunk count), so the divisions run in 32 bits: a 64-bit division is
+  // a long software sequence, and the producer's first copy waits for it.
   __device__ __forceinline__ void init(int64_t c, int64_t step, int radix1, int radix0) {
     r1 = radix1;
     r0 = radix0;
-    const int64_t per2 = static_cast<int64_t>(r1) * r0;
-    d2 = c / per2;
-    const int64_t rem = c - d2 * per2;
-    d1 = static_cast<int>(rem / r0);
-    d0 = static_cast<int>(rem - static_cast<int64_t>(d1) * r0);
-    s2 = step / per2;
-    const int64_t srem = step - s2 * per2;
-    s1 = static_cast<int>(srem / r0);
-    s0 = static_cast<int>(srem - static_cast<int64_t>(s1) * r0);
+    const uint32_t per2 = static_cast<uint32_t>(r1) * static_cast<uint32_t>(r0);
+    const uint32_t c32 = static_cast<uint32_t>(c), st32 = static_cast<uint32_t>(step);
+    const uint32_t q2 = c32 / per2, rem = c32 - q2 * per2;
+    d2 = q2;
+    d1 = static_cast<int>(rem / static_cast<uint32_t>(r0));
+    d0 = static_cast<int>(rem - static_cast<uint32_t>(d1) * static_cast<uint32_t>(r0));
+    const uint32_t t2 = st32 / per2, srem = st32 - t2 * per2;
+    s2 = t2;
+    s1 = static_cast<int>(srem / static_cast<uint32_t>(r0));
+    s0 = static_cast<int>(srem - static_cast<uint32_t>(s1) * static_cast<uint32_t>(r0));
   }
 
   __device__ __forceinline__ void advance() {
@@ -793,7 +797,7 @@ CUtensorMapDataType map_type(int esz) {
                   : (esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
 }
 
-constexpr int64_t kMaxBlocks = (1ll << 31) - 1;  // block coordinates are 32-bit in the walk
+constexpr int64_t kMaxBlocks = (1ll << 31) - 1;  // chunk indices are 32-bit in the walk
 
 }  // namespace
 
@@ -808,6 +812,7 @@ cudaError_t launch_quant_1x128(const void* x, bool f32, int64_t M, int64_t K, in
   const Pipe p{l.status, l.wait_limit_ns, l.debug_skip_fill};
   const int KB = static_cast<int>(K / kTile);
   const int64_t chunks = ((M + rows - 1) / rows) * KB;
+  if (chunks > kMaxBlocks) return cudaErrorInvalidValue;
   if (f32) {
     typename Quant1x128<true>::Args a{chunks, M, K, lds, KB, q, s, pow2};
     return launch_pipe<Quant1x128<true>>(tm, tm, a, p, l.num_sms, stream);
@@ -821,7 +826,7 @@ cudaError_t launch_quant_128x128(const void* w, bool f32, int64_t G, int64_t N, 
   const int esz = f32 ? 4 : 2;
   const int box_rows = f32 ? Quant128x128<true>::kBoxRows : Quant128x128<false>::kBoxRows;
   const int64_t NB = (N + kTile - 1) / kTile, KB = K / kTile;
-  if (N > kMaxBlocks || KB > kMaxBlocks) return cudaErrorInvalidValue;
+  if (N > kMaxBlocks || KB > kMaxBlocks || G * NB * KB > kMaxBlocks) return cudaErrorInvalidValue;
   CUtensorMap tm;
   if (!make_map(&tm, map_type(esz), w, K, N, G, K * esz, N * K * esz, kTile, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
@@ -839,7 +844,7 @@ cudaError_t launch_requant_128x1(const void* src, int src_kind, const float* s_s
                                  int64_t ld_c, int pow2, const QuantLaunch& l, cudaStream_t stream) {
   const int esz = src_kind == 0 ? 1 : (src_kind == 1 ? 2 : 4);
   const int64_t TB = T / kTile, CB = C / kTile;
-  if (TB * CB > kMaxBlocks) return cudaErrorInvalidValue;
+  if (TB * CB > kMaxBlocks || G * TB * CB > kMaxBlocks) return cudaErrorInvalidValue;
   // source as (32-byte column group, token, group, batch); one box is a tile
   const uint64_t cols = 32 / esz;
   const uint64_t dims[4] = {cols, static_cast<uint64_t>(T), static_cast<uint64_t>(C) / cols, static_cast<uint64_t>(G)};
