@@ -664,6 +664,18 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     // BF16 tiles go out through shared-memory staging and TMA stores
     constexpr bool kStage = C::kTmaStore;
     int held = -1;  // pipeline stage kept for staging (kStage, warps < kBorrowWarps)
+    // The previous tile's staging stage, released once this tile's first K
+    // block is promoted: by then its stores have normally read it, so the
+    // wait for that read no longer sits between the epilogue and the next
+    // tile's first promotion (where every warp's buffer release gates the
+    // MMA). The producer needs the stage again only S blocks later.
+    int prev_held = -1;
+    bool prev_staged = false;
+    // (BF16 tiles of the dense and contiguous layouts, where it was
+    // measured faster: 16-block tiles of K=2048 ~4%; FP32 C, whose two
+    // staging rounds per tile already wait on the first round's read, the
+    // masked-rows kernel and the fused quantization were slower with it)
+    constexpr bool kDeferRelease = kStage && !kF32 && !kCompact && !kQ;
     Work wk = work_begin<kSplit>(a);
     Tile ti;
     while (ok && work_next<BN, kSplit, kCompact>(a, wk, ti)) {
@@ -731,6 +743,15 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
           if (!hold) mbar_arrive(empty_bar(s));
           mbar_arrive(tempty_bar(buf));
         }
+        if constexpr (kDeferRelease) {
+          if (prev_held >= 0) {
+            if (lane == 0) {
+              if (prev_staged) bulk_wait_read_all();
+              mbar_arrive(empty_bar(prev_held));
+            }
+            prev_held = -1;
+          }
+        }
       }
       if (!ok) break;
       bool store = !(a.accumulate && ti.kbc == 0);
@@ -779,13 +800,24 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         if (!staged) store_row<NC, kF32>(a, ti, row_in_tile, col0, acc);
       }
       if (held >= 0) {
-        // release the borrowed stage once this warp's stores have read it
-        if (lane == 0) {
-          if (staged) bulk_wait_read_all();
-          mbar_arrive(empty_bar(held));
+        if constexpr (kDeferRelease) {
+          // released after the next tile's first K block (above), or
+          // below if there is none
+          prev_held = held;
+          prev_staged = staged;
+        } else {
+          // release the borrowed stage once this warp's stores have read it
+          if (lane == 0) {
+            if (staged) bulk_wait_read_all();
+            mbar_arrive(empty_bar(held));
+          }
         }
         held = -1;
       }
+    }
+    if (prev_held >= 0 && lane == 0) {
+      if (prev_staged) bulk_wait_read_all();
+      mbar_arrive(empty_bar(prev_held));
     }
     // no store may still be reading shared memory when the CTA exits
     if constexpr (kStage) {
