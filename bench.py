@@ -55,9 +55,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # reported traffic is null. Writes sit below M*N*2 because output lines still
 # in L2 when the kernel ends are written back after it.
 NCU_TRAFFIC = {
-    "kernel_sha": "05c61eeb057f46d2",
-    "per_launch": {2112: 45537536 + 681216, 24576: 212200960 + 180371200,
-                   7168: 83592192 + 37598208, 4096: 60659968 + 11886592},
+    "kernel_sha": "09915b064cc6e4e7",
+    "per_launch": {2112: 45533696 + 564480, 24576: 213175296 + 179571456,
+                   7168: 83422720 + 36988416, 4096: 60712192 + 11744000},
 }
 
 
