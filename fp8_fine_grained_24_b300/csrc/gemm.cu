@@ -93,15 +93,26 @@ struct Cfg {
   static constexpr int kABytes = BM * BK;
   static constexpr int kBBytes = BN * BK;
   static constexpr int kSABytes = BM * 4;
+  // B's scales of the stage's K block: one per column with row scales.
+  // 128x128 block scales reach the promotion warps in one of two ways.
+  // BN=192 and 256 (throughput-bound tiles): the producer copies the K
+  // block's scale of each 128-column block the tile spans into the stage,
+  // so a tile's first K block has nothing to fetch (a 192-wide tile may
+  // start mid-block: two blocks either way). BN=128 (the decode-shaped,
+  // latency-bound K loop, where any addition to a stage's refill showed
+  // up in the time): each promotion warp loads its column block's scales
+  // 128 K blocks at a time into its own staging area.
   static constexpr int kSBBytes = BN * 4;
+  static constexpr bool kProducerScales = (BN != 128);
+  static constexpr int kSbSpan = 2;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kStages * kABytes;
   static constexpr int kOffEpi = kOffB + kStages * kBBytes;     // 1024-aligned (see assert)
   static constexpr int kOffSA = kOffEpi + kEpiBytes;
   static constexpr int kOffSB = kOffSA + kStages * kSABytes;
-  static constexpr int kOffSbw = kOffSB + kStages * kSBBytes;     // per-warp block-scale staging
-  static constexpr int kSbwChunk = 128;                           // K blocks staged at a time
-  static constexpr int kOffBar = kOffSbw + kEpiWarps * kSbwChunk * 4;
+  static constexpr int kOffSbw = kOffSB + kStages * kSBBytes;      // per-warp block-scale staging
+  static constexpr int kSbwChunk = 128;                            // K blocks staged at a time
+  static constexpr int kOffBar = kOffSbw + (kProducerScales ? 0 : kEpiWarps * kSbwChunk * 4);
   // full[S], empty[S], tmem_full[B], tmem_empty[B], drain
   static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 1;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
@@ -535,7 +546,9 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     prefetch_tmap(&tmSA);
     if (kBRow) prefetch_tmap(&tmSB);
     for (int s = 0; s < S; ++s) {
-      mbar_init(full_bar(s), 1);
+      // the producer's expect-tx arrival, and with block scales of B the
+      // arrival of its copies of them (below)
+      mbar_init(full_bar(s), (!kBRow && C::kProducerScales) ? 2 : 1);
       // a stage is free once every promotion warp has seen its K block's MMAs
       // complete (tmem_full) and has read its scales: the MMA issuer does not
       // need to commit to it, which keeps its per-block loop short
@@ -567,6 +580,11 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       Tile ti;
       while (ok && work_next<BN, kSplit, kCompact>(a, wk, ti)) {
         if (ti.skip) continue;
+        // B's block scales of the tile's first 128-column block (BN=192
+        // and 256: the tile spans two)
+        const int nb0 = ti.n0 / 128;
+        const float* sbt = a.sB + static_cast<int64_t>(ti.gB) * a.sb_nblk * a.sb_kblk +
+                           static_cast<int64_t>(nb0) * a.sb_col_stride;
         for (int kb = ti.kb0; kb < ti.kb0 + ti.kbc; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1;
           if (!mbar_wait(empty_bar(s), ph ^ 1, a.status, kStatusTimeoutProducer, a.wait_limit_ns)) {
@@ -588,6 +606,20 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
           tma_load_3d(sbase + C::kOffSA + s * C::kSABytes, &tmSA, full_bar(s), ti.m0, kb, ti.gA);
           if (kBRow)
             tma_load_3d(sbase + C::kOffSB + s * C::kSBBytes, &tmSB, full_bar(s), ti.n0, kb, ti.gB);
+          if constexpr (!kBRow && C::kProducerScales) {
+            // B's 128x128 block scales of this K block, one per 128-column
+            // block of the tile, copied into the stage beside A's scales
+            // (zero for a block past N): the promotion warps read them
+            // there, with nothing to fetch at a tile's first K block
+            const float* sbk = sbt + static_cast<int64_t>(kb) * a.sb_red_stride;
+#pragma unroll
+            for (int j = 0; j < C::kSbSpan; ++j) {
+              const bool in = nb0 + j < a.sb_nblk;
+              cp_async_4(sbase + C::kOffSB + s * C::kSBBytes + j * 4, in ? sbk + j * a.sb_col_stride : a.sB,
+                         in ? 4u : 0u);
+            }
+            cp_async_mbar_arrive_noinc(full_bar(s));
+          }
         }
       }
       // No copy may still be landing in shared memory when the CTA exits:
@@ -596,6 +628,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       for (uint32_t i = first; i < it; ++i) {
         mbar_wait(full_bar(i % S), (i / S) & 1, nullptr, 0, a.wait_limit_ns);
       }
+      cp_async_wait_all();
     }
    } else if (warp == 1 || (C::kMaxIssuers > 1 && warp == 2)) {
     // ------------------------------------------------------------ MMA issuers
@@ -653,9 +686,9 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
     const float* smem_sa = reinterpret_cast<const float*>(smem + C::kOffSA);
     const float* smem_sb = reinterpret_cast<const float*>(smem + C::kOffSB);
-    // Block scales of this warp's column group (inside one 128-column block),
-    // staged 128 K blocks at a time by the warp itself: no cross-warp
-    // barrier that a warp leaving on the error path could leave waiting.
+    // BN=128: block scales of this warp's column group, staged 128 K blocks
+    // at a time by the warp itself (no cross-warp barrier that a warp
+    // leaving on the error path could leave waiting)
     float* sbw = reinterpret_cast<float*>(smem + C::kOffSbw) + ew * C::kSbwChunk;
     float acc[NC];
     uint32_t it = 0;
@@ -682,14 +715,17 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       if (ti.skip) continue;
 #pragma unroll
       for (int j = 0; j < NC; ++j) acc[j] = 0.0f;
-      // K blocks kb0 .. kb0+kbc-1 by their offset jb in the tile's range:
+      // this warp's 128-column block, counted from the tile's first (its
+      // slot among the stage's block scales of B)
+      const int sb_slot = (ti.n0 + col0) / 128 - ti.n0 / 128;
+      // the tile's K blocks kb0 .. kb0+kbc-1 by their offset jb in its range:
       // written this way the loop compiles the same whether kb0 is the
-      // constant 0 (whole tiles) or a Stream-K segment start
+      // constant 0 (whole tiles) or the start of a split's K range
       const int kb0 = ti.kb0, kbc = ti.kbc;
       for (unsigned jb = 0; jb < static_cast<unsigned>(kbc); ++jb, ++it) {
         const uint32_t s = it % S, ph = (it / S) & 1;
         const uint32_t buf = it % NB, tph = (it / NB) & 1;
-        if (!kBRow && (jb % C::kSbwChunk) == 0) {
+        if (!kBRow && !C::kProducerScales && (jb % C::kSbwChunk) == 0) {
           const int nbk = (ti.n0 + col0) / 128;
           const float* src = a.sB + static_cast<int64_t>(ti.gB) * a.sb_nblk * a.sb_kblk +
                              static_cast<int64_t>(nbk) * a.sb_col_stride + static_cast<int64_t>(kb0) * a.sb_red_stride;
@@ -711,7 +747,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         }
         const float sa = smem_sa[s * BM + row_in_tile];
         float sc = 0.0f;
-        if constexpr (!kBRow) sc = sa * sbw[jb % C::kSbwChunk];
+        if constexpr (!kBRow) sc = sa * (C::kProducerScales ? smem_sb[s * BN + sb_slot] : sbw[jb % C::kSbwChunk]);
         const float* sbv = smem_sb + s * BN + col0;
         const uint32_t taddr = tmem_base + lane_bits + buf * BN + col0;
         tc_fence_after();
