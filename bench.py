@@ -55,9 +55,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # reported traffic is null. Writes sit below M*N*2 because output lines still
 # in L2 when the kernel ends are written back after it.
 NCU_TRAFFIC = {
-    "kernel_sha": "09915b064cc6e4e7",
-    "per_launch": {2112: 45533696 + 564480, 24576: 213175296 + 179571456,
-                   7168: 83422720 + 36988416, 4096: 60712192 + 11744000},
+    "kernel_sha": "af4456e1abd2ff85",
+    "per_launch": {2112: 45523456 + 644864, 24576: 212610560 + 179344128,
+                   7168: 83719168 + 36457728, 4096: 60808704 + 11437312},
 }
 
 
