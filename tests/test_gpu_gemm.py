@@ -49,7 +49,10 @@ def test_dense_tiny_config(lib):
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 128), (200, 264, 384), (1, 8, 128), (64, 2112, 1024),
-                                   (300, 520, 640), (513, 768, 256), (128, 7168, 2048)])
+                                   (300, 520, 640), (513, 768, 256), (128, 7168, 2048),
+                                   # one K block per tile on 256-wide tiles (each stage is a
+                                   # tile's first and last), ragged N past the last scale block
+                                   (300, 520, 128), (1500, 1288, 128)])
 def test_dense_shapes(lib, M, N, K):
     _dense_case(lib, M, N, K, seed=M * 7 + N)
 
