@@ -227,11 +227,15 @@ __device__ __forceinline__ Work work_begin(const KArgs& a) {
     w.end = static_cast<int>(e < a.sk_units ? e : a.sk_units);
   } else if constexpr (kSK == kSplitCluster) {
     // cluster t computes tile t; its CTA r (blockIdx.x % cl_split, the
-    // rank: the clusters tile the grid along x) takes the r-th K range
-    const int r = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.cl_split));
-    w.t = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.cl_split));
-    w.u = static_cast<int>(static_cast<int64_t>(r) * a.KB / a.cl_split);
-    w.end = static_cast<int>(static_cast<int64_t>(r + 1) * a.KB / a.cl_split);
+    // rank: the clusters tile the grid along x) takes the r-th K range.
+    // 32-bit unsigned arithmetic (the host splits only K < 2^24 blocks, so
+    // (r + 1) * KB stays below 2^27): a 64-bit division is a long software
+    // sequence ahead of the producer's first copy.
+    const unsigned S = static_cast<unsigned>(a.cl_split), kb = static_cast<unsigned>(a.KB);
+    const unsigned r = blockIdx.x % S;
+    w.t = static_cast<int>(blockIdx.x / S);
+    w.u = static_cast<int>(r * kb / S);
+    w.end = static_cast<int>((r + 1) * kb / S);
   }
   return w;
 }
@@ -1054,6 +1058,7 @@ cudaError_t pick_cluster_split(int mode, int64_t rows, int64_t N, int64_t K, int
   *cl = 0;
   if (mode != kModeDense || groups != 1) return cudaSuccess;
   const int64_t KB = K / BK;
+  if (KB >= (int64_t{1} << 24)) return cudaSuccess;  // the device splits K in 32 bits
   const int64_t tiles = ((rows + BM - 1) / BM) * ((N + 127) / 128);
   if (tiles <= 0 || tiles * 2 > num_sms) return cudaSuccess;
   int64_t S = num_sms / tiles;
