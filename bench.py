@@ -55,9 +55,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # reported traffic is null. Writes sit below M*N*2 because output lines still
 # in L2 when the kernel ends are written back after it.
 NCU_TRAFFIC = {
-    "kernel_sha": "af4456e1abd2ff85",
-    "per_launch": {2112: 45523456 + 644864, 24576: 212610560 + 179344128,
-                   7168: 83719168 + 36457728, 4096: 60808704 + 11437312},
+    "kernel_sha": "78a51e16da86b2ef",
+    "per_launch": {2112: 45531136 + 582912, 24576: 213414656 + 179484416,
+                   7168: 83757824 + 37161216, 4096: 60750592 + 11621632},
 }
 
 
