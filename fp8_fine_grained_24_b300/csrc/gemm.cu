@@ -130,8 +130,11 @@ __device__ __forceinline__ Tile decode_tile(const KArgs& a, int t) {
   Tile ti;
   ti.tile = t;
   ti.sk_start = -1;
+  // Uniform shortcuts for what dense problems (one group) and decode
+  // shapes (one row block) would otherwise divide out: each division is a
+  // dependent instruction sequence ahead of the producer's first copy.
   const int per_group = a.tiles_m * a.tiles_n;
-  const int g = t / per_group;
+  const int g = a.mode == kModeDense ? 0 : t / per_group;
   const int r = t - g * per_group;
   int mb, nb;
   if (a.mode == kModeContig) {
@@ -145,6 +148,9 @@ __device__ __forceinline__ Tile decode_tile(const KArgs& a, int t) {
     const int rr = r - band * kContigBand * a.tiles_n;
     mb = m_first + rr % rows;
     nb = rr / rows;
+  } else if (a.tiles_m == 1) {
+    mb = 0;
+    nb = r;
   } else {
     mb = r % a.tiles_m;
     nb = r / a.tiles_m;
