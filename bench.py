@@ -55,9 +55,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # reported traffic is null. Writes sit below M*N*2 because output lines still
 # in L2 when the kernel ends are written back after it.
 NCU_TRAFFIC = {
-    "kernel_sha": "78a51e16da86b2ef",
-    "per_launch": {2112: 45531136 + 582912, 24576: 213414656 + 179484416,
-                   7168: 83757824 + 37161216, 4096: 60750592 + 11621632},
+    "kernel_sha": "b8b09da913048397",
+    "per_launch": {2112: 45532672 + 573952, 24576: 211239680 + 179841792,
+                   7168: 83652608 + 37178368, 4096: 60663552 + 11681024},
 }
 
 
