@@ -534,7 +534,10 @@ def run_e2e(step, fg, torch, device, steps, barrier):
 # its weight gradient; the 128x1 requantization from E4M3 and from BF16;
 # the small dense case; the prefill GEMM with its output quantized in the
 # epilogue, beside the unfused GEMM + quantizer pair; the data gradient of
-# the N=7168 prefill layer; and the dense weight gradient over 4096 tokens.
+# the N=7168 prefill layer; the dense weight gradient over 4096 tokens; and
+# the prefill step's own quantizations one at a time (1x128 of the 4096 x
+# 7168 activations, 128x128 of each of the four weights), outside the step's
+# per-kernel event windows.
 CONFIG_CASES = (
     ("gemm", (128, 256, 512), None),
     ("gemm", (64, 7168, 16384), None),
@@ -552,6 +555,11 @@ CONFIG_CASES = (
     ("dgrad", (4096, 7168, 7168), None),
     ("wgrad_dense", (4096, 4096, 7168), None),
     ("wgrad_dense_bs", (4096, 4096, 7168), None),
+    ("quant1x128", (4096, 7168), None),
+    ("quant128x128", (2112, 7168), None),
+    ("quant128x128", (24576, 7168), None),
+    ("quant128x128", (7168, 7168), None),
+    ("quant128x128", (4096, 7168), None),
 )
 
 
