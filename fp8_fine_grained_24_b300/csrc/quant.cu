@@ -241,9 +241,10 @@ __device__ __forceinline__ void release(const Slot& sl, int lane) {
 // lanes x 8 elements), so a warp reads 2 rows per shared-memory instruction
 // and writes two 128-byte row segments of q. The scalar work of a tile (the
 // division by 448, the reciprocal) is done once per tile rather than on each
-// of its 16 lanes: the warp's 2*I row maxima are gathered one per lane,
-// every lane computes one scale, and each step fetches its tile's scale by
-// shuffle.
+// of its 16 lanes: a reduce-scatter of the 2*I row maxima over each half's
+// lanes (2I shuffles in all, not 4 per row) leaves every lane one row's
+// maximum, every lane computes that row's scale, and each step fetches its
+// tile's scale by shuffle.
 // BF16: two teams of 8 warps take alternate chunks (I = 8), so that the
 // shuffle and scale chains of one chunk overlap another's; a lane keeps
 // its rows as raw BF16 words, takes the row maxima on packed pairs and
@@ -299,7 +300,7 @@ struct Quant1x128 {
 #pragma unroll
       for (int u = 0; u < kWords; ++u) v[i][u] = *reinterpret_cast<const uint4*>(src + 16 * u);
     }
-    // row maxima: after the xor-shuffles every lane of half h holds am[i] of row 2i+h
+    // the lane's maxima of its kIters rows (row 2i + half for am[i])
     float am[kIters];
 #pragma unroll
     for (int i = 0; i < kIters; ++i) {
@@ -317,30 +318,45 @@ struct Quant1x128 {
         asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m0) : "r"(m1));
         am[i] = fmaxf(__uint_as_float((m0 << 16) & 0x7FFFFFFFu), __uint_as_float(m0 & 0x7FFF0000u));
       }
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) am[i] = fmaxf(am[i], __shfl_xor_sync(0xffffffffu, am[i], o));
     }
+    // Reduce-scatter of the kIters maxima over the 16 lanes of the half:
+    // at lane bit 3, 2, ... the lane with the bit clear keeps the first half
+    // of its values, its partner the second, each taking the max with what
+    // the other sends; the remaining kShift lane bits hold copies of one row
+    // and finish with a plain butterfly. Afterwards lane j of the half holds
+    // the maximum of row 2 * (j >> kShift) + half.
+    constexpr int kLog = kIters == 8 ? 3 : (kIters == 4 ? 2 : (kIters == 2 ? 1 : 0));
+    static_assert((1 << kLog) == kIters, "row count per half");
+    constexpr int kShift = 4 - kLog;
+#pragma unroll
+    for (int r = 0; r < kLog; ++r) {
+      const int bit = 3 - r, n = kIters >> r;
+      const bool upper = (lane >> bit) & 1;
+#pragma unroll
+      for (int q = 0; q < n / 2; ++q) {
+        const float send = upper ? am[q] : am[q + n / 2];
+        const float keep = upper ? am[q + n / 2] : am[q];
+        am[q] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 1 << bit));
+      }
+    }
+#pragma unroll
+    for (int bit = kShift - 1; bit >= 0; --bit) am[0] = fmaxf(am[0], __shfl_xor_sync(0xffffffffu, am[0], 1 << bit));
     release(sl, lane);
-    // lane L takes row t = L % (2I): am[t/2] of half t%2
-    const int t = lane & (kWarpRows - 1);
-    float my_am = 0.0f;
-#pragma unroll
-    for (int i = 0; i < kIters; ++i) {
-      const float x = __shfl_sync(0xffffffffu, am[i], 16 * (t & 1));
-      if ((t >> 1) == i) my_am = x;
-    }
+    const float my_am = am[0];
+    const int my_row = 2 * (j >> kShift) + half;  // of the warp's kWarpRows rows
     const float my_s = tile_scale(my_am, a.pow2 != 0);
     const float my_r = __frcp_rn(my_s);
     const int path = warp_quot_mode(make_tile_div_mode(my_s));
     const int64_t row0 = w.d2 * kRows + wt * kWarpRows;
     const int64_t col = static_cast<int64_t>(w.d0) * kTile;
-    if (lane < kWarpRows && row0 + lane < a.M) a.s[w.d0 * a.lds + row0 + lane] = my_s;
+    if ((j & ((1 << kShift) - 1)) == 0 && row0 + my_row < a.M) a.s[w.d0 * a.lds + row0 + my_row] = my_s;
     uint8_t* qp = a.q + (row0 + half) * a.K + col + j * 8;
     const int64_t rows_left = a.M - row0 - half;
 #pragma unroll
     for (int i = 0; i < kIters; ++i) {
-      const float sc = __shfl_sync(0xffffffffu, my_s, 2 * i + half);
-      const float rc = __shfl_sync(0xffffffffu, my_r, 2 * i + half);
+      // row 2i + half's scale: lane (i << kShift) of this half
+      const float sc = __shfl_sync(0xffffffffu, my_s, 16 * half + (i << kShift));
+      const float rc = __shfl_sync(0xffffffffu, my_r, 16 * half + (i << kShift));
       uint64_t x[4];
       if constexpr (kF32) {
         x[0] = pk2(-__uint_as_float(v[i][0].x), -__uint_as_float(v[i][0].y));
