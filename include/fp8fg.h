@@ -354,6 +354,18 @@ FP8FG_API int fp8fg_study_mma_accumulation(const uint8_t* A, const uint8_t* B, f
  */
 FP8FG_API int fp8fg_debug_set(int key, int64_t value);
 
+/*
+ * Environment variables, read once per process when first needed (tuning
+ * and A/B switches; results stay within the same tolerances):
+ *   FP8FG_BN=128|192|256   tile width of every single-CTA GEMM (default:
+ *                          128 for dense problems of one 128-row block,
+ *                          else 256; MN-major B takes 256 for 192);
+ *   FP8FG_SPLIT=stream|cluster  K split of decode-sized dense GEMMs (key 4);
+ *   FP8FG_PAIR=1           large dense GEMMs on the CTA-pair kernel (key 3);
+ *   FP8FG_ISSUERS=1        one MMA-issuing warp instead of two;
+ *   FP8FG_PDL=0            no programmatic dependent launch.
+ */
+
 #ifdef __cplusplus
 }
 #endif
